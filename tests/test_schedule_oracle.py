@@ -1,0 +1,95 @@
+"""Pins of the schedule oracle (CPU only): the pages' printed orders, full coverage of
+the mask, the pages' qualitative claims (conflict-free shift schedules, shorter critical
+paths), and symmetric-shift balance."""
+import os
+
+import pytest
+
+from oracle import schedule as sc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def read_golden(name):
+    rows = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            w, qs = line.split(":")
+            rows[int(w)] = [int(x) for x in qs.split()]
+    return rows
+
+
+def test_shift_matches_pages_cyclic_example():
+    gold = read_golden("shift_full_N4.txt")
+    for u, qs in gold.items():
+        assert [q for _, q in sc.visits(sc.SHIFT, False, 4, u)] == qs
+        assert all(kv == u for kv, _ in sc.visits(sc.SHIFT, False, 4, u))
+
+
+def test_descending_matches_pages_reversal():
+    gold = read_golden("descending_full_N4.txt")
+    for u, qs in gold.items():
+        assert [q for _, q in sc.visits(sc.DESCENDING, False, 4, u)] == qs
+    assert sc.reduction_order(sc.DESCENDING, False, 4) == sc.reduction_order(sc.SERIAL, False, 4)
+
+
+CASES = [(s, c, n) for n in (2, 4, 6, 8, 16) for s, c in
+         ((sc.SERIAL, False), (sc.SERIAL, True), (sc.DESCENDING, False), (sc.DESCENDING, True),
+          (sc.SHIFT, False), (sc.SYMSHIFT, True))]
+
+
+@pytest.mark.parametrize("sched,causal,N", CASES)
+def test_every_allowed_tile_visited_once(sched, causal, N):
+    seen = []
+    for u in range(sc.num_workers(sched, causal, N)):
+        seen += sc.visits(sched, causal, N, u)
+    want = [(kv, q) for kv in range(N) for q in range(N) if sc.allowed(causal, q, kv)]
+    assert sorted(seen) == sorted(want)
+    order = sc.reduction_order(sched, causal, N)
+    for q in range(N):
+        assert sorted(order[q]) == [kv for kv in range(N) if sc.allowed(causal, q, kv)]
+
+
+@pytest.mark.parametrize("sched,causal,N", CASES)
+def test_conflict_freedom(sched, causal, N):
+    """Shift schedules are conflict-free in lock step (section 2.2 B); the serialized
+    orders are not (every worker wants the same tile at the same step)."""
+    assert sc.conflict_free(sched, causal, N) == (sched in (sc.SHIFT, sc.SYMSHIFT))
+
+
+@pytest.mark.parametrize("N", [2, 4, 8, 16])
+def test_critical_paths(N):
+    """Unit-step critical paths.  Serialized baseline: 2N-1 (the pipeline bubbles of
+    section 1).  Descending helps causal masks only (section 2.2 A); Shift reaches the
+    lower bound N for full masks; Symmetric Shift needs N+1 steps on N/2 workers."""
+    assert sc.critical_path(sc.SERIAL, False, N) == 2 * N - 1
+    assert sc.critical_path(sc.DESCENDING, False, N) == 2 * N - 1
+    assert sc.critical_path(sc.SHIFT, False, N) == N
+    assert sc.critical_path(sc.SERIAL, True, N) == 2 * N - 1
+    assert sc.critical_path(sc.DESCENDING, True, N) == N
+    assert sc.critical_path(sc.SYMSHIFT, True, N) == N + 1
+
+
+@pytest.mark.parametrize("N", [2, 4, 8, 16, 32])
+def test_symshift_balanced_and_one_block_at_a_time(N):
+    """Folding the triangle into a square (section 2.2 B): every worker does N+1 tile
+    steps, and finishes KV block c before it starts block N-1-c."""
+    for c in range(N // 2):
+        seq = sc.visits(sc.SYMSHIFT, True, N, c)
+        assert len(seq) == N + 1
+        kvs = [kv for kv, _ in seq]
+        first_other = kvs.index(N - 1 - c)
+        assert all(kv == c for kv in kvs[:first_other])
+        assert all(kv == N - 1 - c for kv in kvs[first_other:])
+        assert kvs[:N // 2] == [c] * (N // 2)
+        assert all(q >= N // 2 for _, q in seq[:N // 2])      # phase 1: lower-left rectangle
+
+
+def test_symshift_rejects_odd_or_full():
+    with pytest.raises(ValueError):
+        sc.visits(sc.SYMSHIFT, True, 5, 0)
+    with pytest.raises(ValueError):
+        sc.visits(sc.SYMSHIFT, False, 4, 0)
