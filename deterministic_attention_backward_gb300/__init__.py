@@ -1,0 +1,202 @@
+"""Deterministic attention backward (DASH schedules) for NVIDIA GB300, sm_103a.
+
+A thin ctypes binding over ``libdash_attn.so`` (C ABI in ``include/dash_attn.h``).  It
+only marshals arguments: torch tensors supply device memory and the current CUDA stream;
+every step of the forward and backward passes runs in the library's CUDA kernels.  There
+is no fallback: if the library is missing or the GPU is not an sm_103 device the calls
+raise.
+
+    o, lse = fwd(q, k, v, causal=True)
+    dq, dk, dv = bwd(q, k, v, o, do, lse, causal=True, schedule="shift")
+
+Layout BSHD, bf16: q/o/do [B,S,H,D], k/v [B,S,Hkv,D] with H % Hkv == 0 (GQA when
+Hkv < H); lse [B,H,S] fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["fwd", "bwd", "bwd_workspace_bytes", "fwd_workspace_bytes", "status",
+           "sched_table", "SCHEDULES", "lib", "DashError"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdash_attn.so")
+
+SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3}
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+          4: "device-side wait timed out", 5: "workspace missing or too small"}
+EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_workspace_bytes",
+           "dash_attn_bwd", "dash_attn_status", "dash_status_string", "dash_sched_workers",
+           "dash_sched_segments", "dash_sched_steps", "dash_sched_step"]
+
+
+class DashError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)} (status {code})")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with argument types set (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "deterministic_attention_backward_gb300._build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.dash_attn_fwd_workspace_bytes.argtypes = [i, i, i, i]
+        L.dash_attn_fwd_workspace_bytes.restype = sz
+        L.dash_attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+        L.dash_attn_bwd_workspace_bytes.restype = sz
+        L.dash_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+        L.dash_attn_fwd.restype = i
+        L.dash_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i,
+                                    vp, sz, vp]
+        L.dash_attn_bwd.restype = i
+        L.dash_attn_status.argtypes = [vp, vp]
+        L.dash_attn_status.restype = i
+        L.dash_status_string.argtypes = [i]
+        L.dash_status_string.restype = ctypes.c_char_p
+        L.dash_sched_workers.argtypes = [i, i, i]
+        L.dash_sched_workers.restype = i
+        L.dash_sched_segments.argtypes = [i, i, i, i]
+        L.dash_sched_segments.restype = i
+        L.dash_sched_steps.argtypes = [i, i, i, i, i]
+        L.dash_sched_steps.restype = i
+        L.dash_sched_step.argtypes = [i, i, i, i, i, i, ip, ip, ip]
+        L.dash_sched_step.restype = i
+        _lib = L
+        return L
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise DashError(code, where)
+
+
+def _dims(q, k):
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, S, Hkv, D) or Hkv == 0 or H % Hkv:
+        raise ValueError(f"q {tuple(q.shape)} and k {tuple(k.shape)} are not BSHD-compatible")
+    return B, S, H, Hkv, D
+
+
+def _require(t, name, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_ptr(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def fwd_workspace_bytes(B: int, S: int, H: int, D: int) -> int:
+    return int(lib().dash_attn_fwd_workspace_bytes(B, S, H, D))
+
+
+def bwd_workspace_bytes(B: int, S: int, H: int, D: int) -> int:
+    return int(lib().dash_attn_bwd_workspace_bytes(B, S, H, D))
+
+
+def _workspace(nbytes: int, device, workspace=None):
+    import torch
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+        workspace=None, stream=None, check: bool = False):
+    """Attention forward: returns (O [B,S,H,D] bf16, LSE [B,H,S] fp32)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, torch.bfloat16)
+    B, S, H, Hkv, D = _dims(q, k)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    ws = _workspace(fwd_workspace_bytes(B, S, H, D) or 256, q.device, workspace)
+    code = lib().dash_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               l.data_ptr(), B, S, H, H // Hkv, D,
+                               float(scale) if scale else 0.0, int(bool(causal)), ws.data_ptr(),
+                               ws.numel(), _stream_ptr(stream))
+    _check(code, "dash_attn_fwd")
+    if check:
+        status(ws, stream)
+    return o, l
+
+
+def bwd(q, k, v, o, do, lse, causal: bool = False, schedule: str = "shift",
+        scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None,
+        check: bool = False):
+    """Attention backward: returns (dQ, dK, dV) bf16.  ``schedule`` is one of
+    ``atomic`` (non-deterministic reference), ``serial``, ``descending``, ``shift``."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _require(t, n, torch.bfloat16)
+    _require(lse, "lse", torch.float32)
+    B, S, H, Hkv, D = _dims(q, k)
+    if schedule not in SCHEDULES:
+        raise ValueError(f"schedule must be one of {sorted(SCHEDULES)}")
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dv = dv if dv is not None else torch.empty_like(v)
+    need = bwd_workspace_bytes(B, S, H, D)
+    ws = _workspace(need or 256, q.device, workspace)
+    code = lib().dash_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), B, S, H, H // Hkv, D,
+                               float(scale) if scale else 0.0, int(bool(causal)),
+                               SCHEDULES[schedule], ws.data_ptr(),
+                               ws.numel() * ws.element_size(), _stream_ptr(stream))
+    _check(code, "dash_attn_bwd")
+    if check:
+        status(ws, stream)
+    return dq, dk, dv
+
+
+def status(workspace, stream=None):
+    """Synchronise and raise DashError if the last call on ``workspace`` reported a
+    device-side failure (a bounded wait that ran out)."""
+    _check(lib().dash_attn_status(workspace.data_ptr(), _stream_ptr(stream)), "device status")
+
+
+def sched_table(schedule: str, causal: bool, N: int):
+    """The library's schedule as plain lists: per worker, per segment, [(kv, q, rank), ...]."""
+    L = lib()
+    s, m = SCHEDULES[schedule], int(bool(causal))
+    W = L.dash_sched_workers(s, m, N)
+    if W < 0:
+        raise ValueError("unsupported schedule arguments")
+    out = []
+    kv, q, r = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    for w in range(W):
+        segs = []
+        for g in range(L.dash_sched_segments(s, m, N, w)):
+            steps = []
+            for t in range(L.dash_sched_steps(s, m, N, w, g)):
+                _check(L.dash_sched_step(s, m, N, w, g, t, ctypes.byref(kv), ctypes.byref(q),
+                                         ctypes.byref(r)), "dash_sched_step")
+                steps.append((kv.value, q.value, r.value))
+            segs.append(steps)
+        out.append(segs)
+    return out

@@ -1,0 +1,307 @@
+// api.cu -- the extern "C" boundary of libdash_attn.so (declared in include/dash_attn.h):
+// argument validation, workspace carving, TMA descriptor construction and the launch
+// sequence of the forward and backward passes.  No device memory is allocated here.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "dash_attn.h"
+#include "sched.cuh"
+
+namespace {
+
+using dash::kTile;
+
+// ------------------------------------------------------------------ driver entry point
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// [B, S, Hx, D] bf16 viewed as a 3-D tensor (D, Hx, B*S); box = 64 columns x 1 head x 128
+// rows, 128-byte swizzle: one box lands in shared memory as 128 rows of 128 bytes.
+bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int Hx, int D) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hx, (cuuint64_t)B * (cuuint64_t)S};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hx * D * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)dash::kBoxCols, 1, (cuuint32_t)kTile};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ device properties
+struct DevInfo {
+  int sms = 0, major = 0, minor = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+dash_status_t device_info(DevInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DASH_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo &d = g_dev[dev];
+  if (d.sms == 0) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      d.sms = 0;
+      return DASH_ERR_CUDA;
+    }
+  }
+  *out = d;
+  // kernels are built for sm_103a only
+  return (d.major == 10 && d.minor == 3) ? DASH_OK : DASH_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------------------------ validation / workspace
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+dash_status_t check_sizes(int B, int S, int H, int group, int D) {
+  if (B <= 0 || S <= 0 || H <= 0 || group <= 0 || D <= 0) return DASH_ERR_INVALID;
+  if (H % group) return DASH_ERR_INVALID;
+  if (D != 64 && D != 128) return DASH_ERR_UNSUPPORTED;
+  if (S % kTile) return DASH_ERR_UNSUPPORTED;
+  // index arithmetic inside the kernels is 32-bit for row numbers
+  if ((long long)B * S >= (1LL << 31) / 2 || (long long)B * H * (S / kTile) >= (1LL << 30))
+    return DASH_ERR_UNSUPPORTED;
+  return DASH_OK;
+}
+
+constexpr size_t kStatusBytes = 256;
+
+struct BwdWorkspace {
+  uint32_t *status;
+  float *dqacc, *lse2, *dvec;
+  int *sem;
+  size_t dqacc_bytes, sem_bytes, total;
+};
+
+BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
+  BwdWorkspace w{};
+  const size_t rows = (size_t)B * H * S;
+  size_t off = 0;
+  w.status = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + off);
+  off += kStatusBytes;
+  w.dqacc = reinterpret_cast<float *>(static_cast<char *>(ws) + off);
+  w.dqacc_bytes = rows * D * 4;
+  off = align256(off + w.dqacc_bytes);
+  w.lse2 = reinterpret_cast<float *>(static_cast<char *>(ws) + off);
+  off = align256(off + rows * 4);
+  w.dvec = reinterpret_cast<float *>(static_cast<char *>(ws) + off);
+  off = align256(off + rows * 4);
+  w.sem = reinterpret_cast<int *>(static_cast<char *>(ws) + off);
+  w.sem_bytes = (size_t)B * H * (S / kTile) * 4;
+  off = align256(off + w.sem_bytes);
+  w.total = off;
+  return w;
+}
+
+float resolve_scale(float scale, int D) {
+  return scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dash_attn_fwd_workspace_bytes(int B, int S, int H, int D) {
+  if (check_sizes(B, S, H, 1, D) != DASH_OK) return 0;
+  return kStatusBytes;
+}
+
+size_t dash_attn_bwd_workspace_bytes(int B, int S, int H, int D) {
+  if (check_sizes(B, S, H, 1, D) != DASH_OK) return 0;
+  return carve_bwd(nullptr, B, S, H, D).total;
+}
+
+dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int S, int H, int group, int D, float scale,
+                            dash_mask_t mask, void *workspace, size_t workspace_bytes,
+                            dash_stream_t stream) {
+  dash_status_t st = check_sizes(B, S, H, group, D);
+  if (st != DASH_OK) return st;
+  if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
+  if (!q || !k || !v || !o || !lse) return DASH_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return DASH_ERR_INVALID;
+  if (!workspace || workspace_bytes < kStatusBytes || !aligned16(workspace))
+    return DASH_ERR_WORKSPACE;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != DASH_OK) return st;
+  const int Hkv = H / group;
+  CUtensorMap tq, tk, tv;
+  if (!make_bshd_map(&tq, q, B, S, H, D) || !make_bshd_map(&tk, k, B, S, Hkv, D) ||
+      !make_bshd_map(&tv, v, B, S, Hkv, D))
+    return DASH_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return DASH_ERR_CUDA;
+  dash::FwdParams p{};
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.lse = lse;
+  p.status = static_cast<uint32_t *>(workspace);
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = group;
+  p.N = S / kTile;
+  p.causal = mask == DASH_MASK_CAUSAL;
+  p.scale_log2 = resolve_scale(scale, D) * dash::kLog2e;
+  return dash::launch_fwd(D, tq, tk, tv, p, s) == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                            int B, int S, int H, int group, int D, float scale,
+                            dash_mask_t mask, dash_sched_t sched, void *workspace,
+                            size_t workspace_bytes, dash_stream_t stream) {
+  dash_status_t st = check_sizes(B, S, H, group, D);
+  if (st != DASH_OK) return st;
+  if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
+  if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_SHIFT) return DASH_ERR_INVALID;
+  const void *ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
+  for (const void *ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return DASH_ERR_INVALID;
+  const int N = S / kTile;
+  const int causal = mask == DASH_MASK_CAUSAL;
+  if (sched == DASH_SCHED_SHIFT && causal && (N % 2)) return DASH_ERR_UNSUPPORTED;
+  const BwdWorkspace need = carve_bwd(nullptr, B, S, H, D);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need.total)
+    return DASH_ERR_WORKSPACE;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != DASH_OK) return st;
+  const int Hkv = H / group;
+  const int workers = dash::sched_workers(sched, causal, N);
+  const long long total_units = (long long)B * Hkv * workers;
+  const int grid = (int)(total_units < dev.sms ? total_units : dev.sms);
+  // every worker of a head must be resident at once for the shift schedules
+  if (sched == DASH_SCHED_SHIFT && workers > grid) return DASH_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_bshd_map(&tq, q, B, S, H, D) || !make_bshd_map(&tk, k, B, S, Hkv, D) ||
+      !make_bshd_map(&tv, v, B, S, Hkv, D) || !make_bshd_map(&tdo, dout, B, S, H, D))
+    return DASH_ERR_CUDA;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const BwdWorkspace w = carve_bwd(workspace, B, S, H, D);
+  const float sc = resolve_scale(scale, D);
+  // status word + dQ accumulator are contiguous; semaphores separately
+  if (cudaMemsetAsync(w.status, 0, kStatusBytes + w.dqacc_bytes, s) != cudaSuccess ||
+      cudaMemsetAsync(w.sem, 0, w.sem_bytes, s) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  if (dash::launch_preprocess(static_cast<const __nv_bfloat16 *>(o),
+                              static_cast<const __nv_bfloat16 *>(dout), lse, w.dvec, w.lse2, B, S,
+                              H, D, s) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  dash::BwdParams p{};
+  p.lse2 = w.lse2;
+  p.dvec = w.dvec;
+  p.dqacc = w.dqacc;
+  p.sem = w.sem;
+  p.status = w.status;
+  p.dk = static_cast<__nv_bfloat16 *>(dk);
+  p.dv = static_cast<__nv_bfloat16 *>(dv);
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = group;
+  p.N = N;
+  p.sched = sched;
+  p.causal = causal;
+  p.workers = workers;
+  p.total_units = (int)total_units;
+  p.scale_log2 = sc * dash::kLog2e;
+  p.scale = sc;
+  if (dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC, tq, tk, tv, tdo, p, grid, s) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  if (dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, s) !=
+      cudaSuccess)
+    return DASH_ERR_CUDA;
+  return DASH_OK;
+}
+
+dash_status_t dash_attn_status(void *workspace, dash_stream_t stream) {
+  if (!workspace) return DASH_ERR_INVALID;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  if (word & (dash::kErrMbarTimeout | dash::kErrSemTimeout | dash::kErrAborted))
+    return DASH_ERR_TIMEOUT;
+  if (word) return DASH_ERR_CUDA;
+  return DASH_OK;
+}
+
+const char *dash_status_string(dash_status_t s) {
+  switch (s) {
+    case DASH_OK:
+      return "ok";
+    case DASH_ERR_INVALID:
+      return "invalid argument";
+    case DASH_ERR_UNSUPPORTED:
+      return "unsupported configuration";
+    case DASH_ERR_CUDA:
+      return "CUDA error";
+    case DASH_ERR_TIMEOUT:
+      return "device-side wait timed out";
+    case DASH_ERR_WORKSPACE:
+      return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+// ------------------------------------------------------------------ schedule queries
+static bool sched_args_ok(int sched, int mask, int N) {
+  if (sched < 0 || sched > 3 || (mask != 0 && mask != 1) || N <= 0) return false;
+  if (sched == DASH_SCHED_SHIFT && mask == 1 && (N % 2)) return false;
+  return true;
+}
+
+int dash_sched_workers(int sched, int mask, int N) {
+  return sched_args_ok(sched, mask, N) ? dash::sched_workers(sched, mask, N) : -1;
+}
+
+int dash_sched_segments(int sched, int mask, int N, int worker) {
+  if (!sched_args_ok(sched, mask, N) || worker < 0 || worker >= dash::sched_workers(sched, mask, N))
+    return -1;
+  return dash::sched_segments(sched, mask);
+}
+
+int dash_sched_steps(int sched, int mask, int N, int worker, int segment) {
+  const int nseg = dash_sched_segments(sched, mask, N, worker);
+  if (nseg < 0 || segment < 0 || segment >= nseg) return -1;
+  return dash::seg_steps(sched, mask, N, worker, segment);
+}
+
+int dash_sched_step(int sched, int mask, int N, int worker, int segment, int step, int *kv,
+                    int *q, int *rank) {
+  const int n = dash_sched_steps(sched, mask, N, worker, segment);
+  if (n < 0 || step < 0 || step >= n) return -1;
+  const int kvb = dash::seg_kv(sched, mask, N, worker, segment);
+  const int qt = dash::step_q(sched, mask, N, worker, segment, step);
+  if (kv) *kv = kvb;
+  if (q) *q = qt;
+  if (rank) *rank = dash::dq_rank(sched, mask, N, qt, kvb);
+  return 0;
+}
+
+}  // extern "C"

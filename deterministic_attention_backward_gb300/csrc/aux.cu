@@ -1,0 +1,118 @@
+// aux.cu -- the two memory-bound companions of the backward tile kernel:
+//   preprocess:  Dvec[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]   (fp32)
+//                lse2[b,h,i] = LSE[b,h,i] * log2(e)              (exp2-domain LSE)
+//   dq_convert:  dQ[b,i,h,:] = bf16_rne(scale * dQacc)            (tile-native -> BSHD)
+#include "common.cuh"
+
+namespace dash {
+namespace {
+
+// One warp per (b, i, h) row; rows enumerated in BSHD order so the O/dO reads of a CTA are
+// one contiguous range.
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16 *__restrict__ o,
+                                                         const __nv_bfloat16 *__restrict__ dout,
+                                                         const float *__restrict__ lse,
+                                                         float *__restrict__ dvec,
+                                                         float *__restrict__ lse2, int B, int S,
+                                                         int H) {
+  constexpr int kPer = D / 32;  // bf16 elements per lane (2 or 4)
+  const long long rows = (long long)B * S * H;
+  const int lane = threadIdx.x & 31;
+  for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows;
+       row += (long long)gridDim.x * 8) {
+    const __nv_bfloat16 *po = o + row * D + lane * kPer;
+    const __nv_bfloat16 *pd = dout + row * D + lane * kPer;
+    float acc = 0.f;
+    if constexpr (kPer == 4) {
+      const uint2 a = *reinterpret_cast<const uint2 *>(po);
+      const uint2 c = *reinterpret_cast<const uint2 *>(pd);
+      const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
+      const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&c);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(c2[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    } else {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(po));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pd));
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      const int h = (int)(row % H);
+      const long long bi = row / H;
+      const int i = (int)(bi % S);
+      const int b = (int)(bi / S);
+      const size_t r = ((size_t)b * H + h) * S + i;
+      dvec[r] = acc;
+      lse2[r] = lse[r] * kLog2e;
+    }
+  }
+}
+
+// One thread per 4 output elements; the 4-column chunk index runs fastest so a warp
+// writes contiguous bf16 rows.  dQacc layout: [B,H,N][D/4][128][4].
+template <int D>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
+                                                         __nv_bfloat16 *__restrict__ dq,
+                                                         float scale, int B, int S, int H) {
+  constexpr int C4 = D / 4;
+  const int N = S / kTile;
+  const long long total = (long long)B * H * N * kTile * C4;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int c4 = (int)(idx % C4);
+    const int r = (int)((idx / C4) % kTile);
+    const long long t = idx / ((long long)C4 * kTile);  // (b*H + h)*N + i
+    const int i = (int)(t % N);
+    const long long bh = t / N;
+    const int h = (int)(bh % H);
+    const int b = (int)(bh / H);
+    const float4 v = *reinterpret_cast<const float4 *>(acc + ((t * C4 + c4) * kTile + r) * 4);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t *>(&lo);
+    packed.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(dq + (((size_t)b * S + (size_t)i * kTile + r) * H + h) * D +
+                               4 * c4) = packed;
+  }
+}
+
+int grid_for(long long work, int per_block, int cap) {
+  long long g = (work + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  return (int)(g > cap ? cap : g);
+}
+
+}  // namespace
+
+cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout, const float *lse,
+                              float *dvec, float *lse2, int B, int S, int H, int D,
+                              cudaStream_t stream) {
+  const long long rows = (long long)B * S * H;
+  const int grid = grid_for(rows, 8, 152 * 16);
+  if (D == 64)
+    preprocess_kernel<64><<<grid, 256, 0, stream>>>(o, dout, lse, dvec, lse2, B, S, H);
+  else
+    preprocess_kernel<128><<<grid, 256, 0, stream>>>(o, dout, lse, dvec, lse2, B, S, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B, int S,
+                              int H, int D, cudaStream_t stream) {
+  const long long work = (long long)B * H * S * (D / 4);
+  const int grid = grid_for(work, 256, 152 * 32);
+  if (D == 64)
+    dq_convert_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+  else
+    dq_convert_kernel<128><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+  return cudaGetLastError();
+}
+
+}  // namespace dash

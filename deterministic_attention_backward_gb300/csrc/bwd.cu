@@ -1,0 +1,556 @@
+// bwd.cu -- the deterministic attention backward tile kernel (the DASH hot path).
+//
+// One persistent CTA per SM executes *workers* (sched.cuh): a worker owns one KV block j
+// (or the pair c, N-1-c) of one (batch, kv head), keeps dK_j/dV_j in tensor memory for
+// the whole segment (gist.science technical summary, section 2.1: one KV tile's
+// operations run back to back on one SM with on-chip accumulation) and visits query
+// tiles in the order of the selected schedule (section 2.2).  Per visited tile (128 query
+// rows i, all in one query head h) it runs the five dense contractions on the tcgen05
+// tensor cores:
+//   G1  S^T  = K_j Q_i^T                   (128 x 128 x D)  -> TMEM
+//   G2  dP^T = V_j dO_i^T                  (128 x 128 x D)  -> TMEM
+//       P^T  = exp2(S^T * scale*log2e - LSE_i*log2e)   [causal: 0 above the diagonal]
+//       dS^T = P^T o (dP^T - Dvec_i)                    (softmax-gradient warpgroups)
+//   G3  dV_j += P^T dO_i                   (128 x D x 128)  A = P^T from TMEM
+//   G4  dK_j += dS^T Q_i                   (128 x D x 128)  A = dS^T from TMEM
+//   G5  dQ_part = dS K_j                   (128 x D x 128)  A = dS from shared memory
+// and the epilogue warpgroup adds dQ_part into the fp32 dQ accumulator.  In the
+// deterministic modes the addition into dQ tile (b,h,i) happens only when that tile's
+// ordering semaphore equals this worker's rank in the tile's accumulation order, and the
+// semaphore is advanced after the addition is globally visible (section 1: the dQ
+// accumulation order is fixed; the schedules decide which order and how much waiting it
+// costs).  In the atomic mode the additions are unordered.
+//
+// Warp roles (512 threads):
+//   warp 0      TMA producer (one lane): K_j, V_j per segment; Q_i, dO_i, LSE_i, Dvec_i
+//               per step into a ring of shared-memory stages
+//   warp 1      MMA issuer (one lane): G1..G5, tcgen05.commit to mbarriers
+//   warp 2      allocates / frees the 512 TMEM columns
+//   warps 4-11  two softmax-gradient warpgroups; warpgroup w handles query columns
+//               [64w, 64w+64) of the tile, thread = KV row (TMEM lane)
+//   warps 12-15 epilogue warpgroup: dQ partial TMEM -> ordered/atomic fp32 reduction in
+//               global memory; dK/dV TMEM -> bf16 at the end of each segment
+// TMEM columns: S^T/P^T [0,128), dP^T/dS^T and the dQ partial [128,256), dK [256,256+D),
+// dV [256+D, 256+2D).
+#include "common.cuh"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace dash {
+namespace {
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kTileBytes = D * kTile * 2;  // one [128 x D] bf16 tile
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // Q_i and dO_i
+  static constexpr int offK = 0;
+  static constexpr int offV = kTileBytes;
+  static constexpr int offStage = 2 * kTileBytes;  // stage s: Q at +s*kStageBytes, dO after
+  static constexpr int offDS = offStage + kStages * kStageBytes;
+  static constexpr int kDSBytes = kTile * kTile * 2;
+  static constexpr int offLSE = offDS + kDSBytes;
+  static constexpr int offDVEC = offLSE + kStages * kTile * 4;
+  static constexpr int offBar = offDVEC + kStages * kTile * 4;
+  static constexpr int kNumBars = 2 * kStages + 9;
+  static constexpr int offMisc = offBar + kNumBars * 8;
+  static constexpr int kBytes = offMisc + 32;
+  static constexpr uint32_t tS = 0, tDP = 128, tDQ = 128, tDK = 256, tDV = 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kBytes <= 232448, "shared memory budget");
+  static_assert(offDS % 1024 == 0 && offStage % 1024 == 0, "swizzle atoms need 1 KB alignment");
+};
+
+struct Unit {
+  int b, hkv, w;
+};
+__device__ __forceinline__ Unit decode_unit(const BwdParams &p, int u) {
+  Unit r;
+  r.w = u % p.workers;
+  const int bh = u / p.workers;
+  r.hkv = bh % p.Hkv;
+  r.b = bh / p.Hkv;
+  return r;
+}
+
+template <int D>
+struct Bars {
+  uint64_t *full, *empty, *kv_full, *kv_empty, *sdp_full, *p_ready, *g5_done, *dq_empty,
+      *dkv_full, *dkv_empty, *drain;
+  __device__ explicit Bars(uint8_t *smem) {
+    using L = BwdLayout<D>;
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + L::offBar);
+    full = b;
+    empty = b + L::kStages;
+    b += 2 * L::kStages;
+    kv_full = b + 0;
+    kv_empty = b + 1;
+    sdp_full = b + 2;
+    p_ready = b + 3;
+    g5_done = b + 4;
+    dq_empty = b + 5;
+    dkv_full = b + 6;
+    dkv_empty = b + 7;
+    drain = b + 8;
+  }
+};
+
+// ---------------------------------------------------------------------------------------
+template <int D>
+__device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
+                             const CUtensorMap *tdo, const BwdParams &p, uint8_t *smem,
+                             const Bars<D> &bar, const Abort &ab) {
+  using L = BwdLayout<D>;
+  uint32_t it = 0, seg_it = 0;
+  int last_full[L::kStages];
+#pragma unroll
+  for (int s = 0; s < L::kStages; ++s) last_full[s] = -1;
+  int last_kv = -1;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+    const Unit un = decode_unit(p, u);
+    const int nseg = sched_segments(p.sched, p.causal);
+    for (int seg = 0; ok && seg < nseg; ++seg) {
+      const int kv = seg_kv(p.sched, p.causal, p.N, un.w, seg);
+      const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg);
+      if (!mbar_wait(bar.kv_empty, (seg_it & 1) ^ 1, ab)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(bar.kv_full, 2 * L::kTileBytes);
+      const int krow = un.b * p.S + kv * kTile;
+#pragma unroll
+      for (int bx = 0; bx < L::kBoxes; ++bx) {
+        tma_load_3d(smem + L::offK + bx * kBoxBytes, tk, bar.kv_full, bx * kBoxCols, un.hkv, krow);
+        tma_load_3d(smem + L::offV + bx * kBoxBytes, tv, bar.kv_full, bx * kBoxCols, un.hkv, krow);
+      }
+      last_kv = seg_it & 1;
+      ++seg_it;
+      for (int g = 0; ok && g < p.G; ++g) {
+        const int h = un.hkv * p.G + g;
+        for (int t = 0; t < nsteps; ++t) {
+          const int q = step_q(p.sched, p.causal, p.N, un.w, seg, t);
+          const int s = it % L::kStages;
+          const uint32_t ph = (it / L::kStages) & 1;
+          if (!mbar_wait(&bar.empty[s], ph ^ 1, ab)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar.full[s], L::kStageBytes + 2 * kTile * 4);
+          const int qrow = un.b * p.S + q * kTile;
+          uint8_t *sq = smem + L::offStage + s * L::kStageBytes;
+#pragma unroll
+          for (int bx = 0; bx < L::kBoxes; ++bx) {
+            tma_load_3d(sq + bx * kBoxBytes, tq, &bar.full[s], bx * kBoxCols, h, qrow);
+            tma_load_3d(sq + L::kTileBytes + bx * kBoxBytes, tdo, &bar.full[s], bx * kBoxCols, h,
+                        qrow);
+          }
+          const size_t roff = (size_t)(un.b * p.H + h) * p.S + (size_t)q * kTile;
+          bulk_load(smem + L::offLSE + s * kTile * 4, p.lse2 + roff, kTile * 4, &bar.full[s]);
+          bulk_load(smem + L::offDVEC + s * kTile * 4, p.dvec + roff, kTile * 4, &bar.full[s]);
+          last_full[s] = (int)ph;
+          ++it;
+        }
+      }
+    }
+  }
+  if (!ok) {  // leave no copy in flight into shared memory
+#pragma unroll
+    for (int s = 0; s < L::kStages; ++s)
+      if (last_full[s] >= 0) mbar_wait_drain(&bar.full[s], (uint32_t)last_full[s], 100000000ull);
+    if (last_kv >= 0) mbar_wait_drain(bar.kv_full, (uint32_t)last_kv, 100000000ull);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+template <int D>
+__device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D> &bar,
+                        const Abort &ab) {
+  using L = BwdLayout<D>;
+  constexpr uint32_t kIdescSS = make_idesc_bf16(128, 128, false, false);  // G1, G2
+  constexpr uint32_t kIdescTS = make_idesc_bf16(128, D, false, true);     // G3, G4
+  constexpr uint32_t kIdescG5 = make_idesc_bf16(128, D, true, true);      // G5
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t it = 0, seg_it = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+    const Unit un = decode_unit(p, u);
+    const int nseg = sched_segments(p.sched, p.causal);
+    for (int seg = 0; ok && seg < nseg; ++seg) {
+      const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg) * p.G;
+      if (!mbar_wait(bar.kv_full, seg_it & 1, ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int st = 0; st < nsteps; ++st, ++it) {
+        const int s = it % L::kStages;
+        const uint32_t ph = (it / L::kStages) & 1;
+        if (!mbar_wait(&bar.full[s], ph, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t aQ = sbase + L::offStage + s * L::kStageBytes;
+        const uint32_t aDO = aQ + L::kTileBytes;
+        // G1: S^T = K_j Q_i^T  (contraction over D; both operands K-major)
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t koff = (k >> 2) * kBoxBytes + (k & 3) * 32;
+          mma_ss(tmem + L::tS, make_sdesc_sw128(sbase + L::offK + koff, 16, 1024),
+                 make_sdesc_sw128(aQ + koff, 16, 1024), kIdescSS, k > 0);
+        }
+        // the dP^T columns also hold the previous step's dQ partial: wait until drained
+        if (it > 0) {
+          if (!mbar_wait(bar.dq_empty, (it - 1) & 1, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        // G2: dP^T = V_j dO_i^T
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t koff = (k >> 2) * kBoxBytes + (k & 3) * 32;
+          mma_ss(tmem + L::tDP, make_sdesc_sw128(sbase + L::offV + koff, 16, 1024),
+                 make_sdesc_sw128(aDO + koff, 16, 1024), kIdescSS, k > 0);
+        }
+        mma_commit(bar.sdp_full);
+        if (!mbar_wait(bar.p_ready, it & 1, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool first = (st == 0);
+        if (first && seg_it > 0) {  // previous segment's dK/dV must have been read out
+          if (!mbar_wait(bar.dkv_empty, (seg_it - 1) & 1, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        // G3: dV_j += P^T dO_i ; G4: dK_j += dS^T Q_i  (contraction over the 128 query rows;
+        // A from TMEM, B MN-major).  P^T / dS^T of query columns [64w, 64w+64) sit packed
+        // (bf16x2) in columns [64w, 64w+32) of their region.
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t pcol = (k < 4) ? 8 * k : 64 + 8 * (k - 4);
+          const uint32_t moff = k * 2048;
+          const uint32_t acc = (first && k == 0) ? 0u : 1u;
+          mma_ts(tmem + L::tDV, tmem + L::tS + pcol,
+                 make_sdesc_sw128(aDO + moff, kBoxBytes, 1024), kIdescTS, acc);
+          mma_ts(tmem + L::tDK, tmem + L::tDP + pcol, make_sdesc_sw128(aQ + moff, kBoxBytes, 1024),
+                 kIdescTS, acc);
+        }
+        mma_commit(&bar.empty[s]);
+        // G5: dQ_part = dS K_j  (contraction over the 128 KV rows; both operands MN-major)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t moff = k * 2048;
+          mma_ss(tmem + L::tDQ, make_sdesc_sw128(sbase + L::offDS + moff, kBoxBytes, 1024),
+                 make_sdesc_sw128(sbase + L::offK + moff, kBoxBytes, 1024), kIdescG5, k > 0);
+        }
+        mma_commit(bar.g5_done);
+        if (st == nsteps - 1) {
+          mma_commit(bar.kv_empty);
+          mma_commit(bar.dkv_full);
+        }
+      }
+      ++seg_it;
+    }
+  }
+  // leave no MMA in flight
+  mma_commit(bar.drain);
+  mbar_wait_drain(bar.drain, 0, 100000000ull);
+}
+
+// ---------------------------------------------------------------------------------------
+template <int D>
+__device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tmem,
+                                 const Bars<D> &bar, const Abort &ab) {
+  using L = BwdLayout<D>;
+  const int warp = warp_id(), lane = lane_id();
+  const int wg = (warp - 4) >> 2;  // 0 or 1: query columns [64 wg, 64 wg + 64)
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;  // KV row of this thread = TMEM lane
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const int c0 = wg * 64;
+  uint8_t *ds_row = smem + L::offDS + wg * kBoxBytes + r * 128;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+    const Unit un = decode_unit(p, u);
+    const int nseg = sched_segments(p.sched, p.causal);
+    for (int seg = 0; ok && seg < nseg; ++seg) {
+      const int kv = seg_kv(p.sched, p.causal, p.N, un.w, seg);
+      const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg);
+      for (int g = 0; ok && g < p.G; ++g) {
+        for (int t = 0; t < nsteps; ++t, ++it) {
+          const int q = step_q(p.sched, p.causal, p.N, un.w, seg, t);
+          const bool diag = p.causal && (q == kv);
+          const int s = it % L::kStages;
+          const uint32_t ph = (it / L::kStages) & 1;
+          if (!mbar_wait_warp(bar.sdp_full, it & 1, ab) || !mbar_wait_warp(&bar.full[s], ph, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float *lse_s = reinterpret_cast<const float *>(smem + L::offLSE + s * kTile * 4);
+          const float *dvec_s = reinterpret_cast<const float *>(smem + L::offDVEC + s * kTile * 4);
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const int col = c0 + ch * 32;
+            uint32_t sv[32], dpv[32];
+            tmem_ld32(tmem + lane_off + L::tS + col, sv);
+            tmem_ld32(tmem + lane_off + L::tDP + col, dpv);
+            tmem_ld_wait();
+            uint32_t pk[16], dk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + col + c);
+              const float4 d4 = *reinterpret_cast<const float4 *>(dvec_s + col + c);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+              float pe[4], ds[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float x = fmaf(__uint_as_float(sv[c + e]), p.scale_log2, -lv[e]);
+                float pv = ex2_approx(x);
+                if (diag && (col + c + e) < r) pv = 0.f;
+                pe[e] = pv;
+                ds[e] = pv * (__uint_as_float(dpv[c + e]) - dvv[e]);
+              }
+              pk[c / 2] = pack_bf16(pe[0], pe[1]);
+              pk[c / 2 + 1] = pack_bf16(pe[2], pe[3]);
+              dk[c / 2] = pack_bf16(ds[0], ds[1]);
+              dk[c / 2 + 1] = pack_bf16(ds[2], ds[3]);
+            }
+            // P^T and dS^T (bf16x2) into the columns this thread has already read
+            tmem_st16(tmem + lane_off + L::tS + c0 + ch * 16, pk);
+            tmem_st16(tmem + lane_off + L::tDP + c0 + ch * 16, dk);
+            // dS into shared memory as the MN-major A operand of G5: row r of box wg,
+            // 16-byte chunk (4ch + j) at position (4ch + j) ^ (r % 8)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int cj = ch * 4 + j;
+              *reinterpret_cast<uint4 *>(ds_row + ((cj ^ (r & 7)) << 4)) =
+                  make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar.p_ready);
+            mbar_arrive(&bar.empty[s]);
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+template <int D, bool DET>
+__device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D> &bar,
+                             const Abort &ab) {
+  using L = BwdLayout<D>;
+  const int warp = warp_id(), lane = lane_id();
+  const int et = threadIdx.x - 12 * 32;  // 0..127
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;  // query row (dQ) or KV row (dK/dV) = TMEM lane
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  volatile int *decision = reinterpret_cast<volatile int *>(smem + L::offMisc + 8);  // [2]
+  uint32_t it = 0, seg_it = 0, dec = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+    const Unit un = decode_unit(p, u);
+    const int nseg = sched_segments(p.sched, p.causal);
+    for (int seg = 0; ok && seg < nseg; ++seg) {
+      const int kv = seg_kv(p.sched, p.causal, p.N, un.w, seg);
+      const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg);
+      for (int g = 0; ok && g < p.G; ++g) {
+        const int h = un.hkv * p.G + g;
+        for (int t = 0; t < nsteps; ++t, ++it) {
+          const int q = step_q(p.sched, p.causal, p.N, un.w, seg, t);
+          const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
+          int *sem = p.sem + tile_idx;
+          const int rank = dq_rank(p.sched, p.causal, p.N, q, kv);
+          if (et == 0) {
+            bool w = mbar_wait(bar.g5_done, it & 1, ab);
+            if (DET && w) w = sem_wait(sem, rank, ab);
+            decision[dec & 1] = w ? 1 : 0;
+          }
+          named_bar_sync(1, 128);
+          if (!decision[dec & 1]) {
+            ok = false;
+            break;
+          }
+          ++dec;
+          tc_fence_after();
+          float *tile = p.dqacc + tile_idx * (size_t)(kTile * D);
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + L::tDQ + ch * 32, v);
+            tmem_ld_wait();
+            if (ch == D / 32 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar.dq_empty);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int c4 = ch * 8 + j;
+              red_add_v4(tile + ((size_t)c4 * kTile + r) * 4, __uint_as_float(v[4 * j]),
+                         __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                         __uint_as_float(v[4 * j + 3]));
+            }
+          }
+          if (DET) {
+            fence_acq_rel_gpu();
+            named_bar_sync(1, 128);
+            if (et == 0) st_release_gpu(sem, rank + 1);
+          }
+        }
+      }
+      if (!ok) break;
+      // segment end: dK_j (scaled) and dV_j to bf16
+      if (et == 0) decision[dec & 1] = mbar_wait(bar.dkv_full, seg_it & 1, ab) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!decision[dec & 1]) {
+        ok = false;
+        break;
+      }
+      ++dec;
+      tc_fence_after();
+      const size_t orow = ((size_t)(un.b * p.S + kv * kTile + r) * p.Hkv + un.hkv) * D;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t kk[32], vv[32];
+        tmem_ld32(tmem + lane_off + L::tDK + ch * 32, kk);
+        tmem_ld32(tmem + lane_off + L::tDV + ch * 32, vv);
+        tmem_ld_wait();
+        if (ch == D / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar.dkv_empty);
+        }
+        uint32_t kp[16], vp[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          kp[m] = pack_bf16(__uint_as_float(kk[2 * m]) * p.scale,
+                            __uint_as_float(kk[2 * m + 1]) * p.scale);
+          vp[m] = pack_bf16(__uint_as_float(vv[2 * m]), __uint_as_float(vv[2 * m + 1]));
+        }
+        uint4 *dkp = reinterpret_cast<uint4 *>(p.dk + orow + ch * 32);
+        uint4 *dvp = reinterpret_cast<uint4 *>(p.dv + orow + ch * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          dkp[j] = make_uint4(kp[4 * j], kp[4 * j + 1], kp[4 * j + 2], kp[4 * j + 3]);
+          dvp[j] = make_uint4(vp[4 * j], vp[4 * j + 1], vp[4 * j + 2], vp[4 * j + 3]);
+        }
+      }
+      ++seg_it;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+template <int D, bool DET>
+__global__ void __launch_bounds__(512, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kErrSmemAlign);
+    return;
+  }
+  const Bars<D> bar(smem);
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L::offMisc);
+  int *s_abort = reinterpret_cast<int *>(smem + L::offMisc + 4);
+  const Abort ab{s_abort, p.status};
+  const int warp = warp_id(), lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(&bar.full[s], 1);
+      mbar_init(&bar.empty[s], 1 + 8);  // MMA commit + 8 softmax-gradient warps
+    }
+    mbar_init(bar.kv_full, 1);
+    mbar_init(bar.kv_empty, 1);
+    mbar_init(bar.sdp_full, 1);
+    mbar_init(bar.p_ready, 8);
+    mbar_init(bar.g5_done, 1);
+    mbar_init(bar.dq_empty, 4);
+    mbar_init(bar.dkv_full, 1);
+    mbar_init(bar.dkv_empty, 4);
+    mbar_init(bar.drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 2) {
+    tmem_alloc(s_tmem, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
+  } else if (warp == 1) {
+    if (lane == 0) bwd_mma<D>(p, smem, tmem, bar, ab);
+  } else if (warp >= 4 && warp < 12) {
+    bwd_softmax_grad<D>(p, smem, tmem, bar, ab);
+  } else if (warp >= 12) {
+    bwd_epilogue<D, DET>(p, smem, tmem, bar, ab);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D, bool DET>
+cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const CUtensorMap &tdo, const BwdParams &p, int grid, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  auto kern = bwd_kernel<D, DET>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 512, L::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_smem_bytes(int D) {
+  return D == 64 ? BwdLayout<64>::kBytes : BwdLayout<128>::kBytes;
+}
+
+cudaError_t launch_bwd(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, int grid,
+                       cudaStream_t stream) {
+  if (D == 64)
+    return deterministic ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, grid, stream)
+                         : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, grid, stream);
+  return deterministic ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, grid, stream)
+                       : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, grid, stream);
+}
+
+}  // namespace dash

@@ -1,0 +1,65 @@
+// common.cuh -- constants, parameter blocks and the internal launch interface shared by the
+// translation units of libdash_attn.so.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dash {
+
+constexpr int kTile = 128;                // rows of a query tile and of a KV block
+constexpr int kBoxCols = 64;              // bf16 columns of one 128-byte-swizzled box
+constexpr int kBoxBytes = kTile * 128;    // one [128 x 64] bf16 box = 16 KB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// error codes written into a workspace status word (bit flags)
+enum : uint32_t {
+  kErrMbarTimeout = 1u,  // an mbarrier phase never completed
+  kErrSemTimeout = 2u,   // a dQ ordering semaphore never reached the expected rank
+  kErrSmemAlign = 4u,    // dynamic shared memory not 1024-byte aligned
+  kErrAborted = 8u,      // the CTA stopped because another CTA reported an error
+};
+
+// Backward kernel parameters (besides the TMA descriptors of Q, K, V, dO).
+struct BwdParams {
+  const float *lse2;  // [B,H,S]  LSE * log2(e)
+  const float *dvec;  // [B,H,S]  rowsum(dO * O)
+  float *dqacc;       // fp32 dQ accumulator, tile-native layout [B,H,N][D/4][128][4]
+  int *sem;           // [B,H,N] dQ ordering semaphores (number of partials added so far)
+  uint32_t *status;   // status word (error bit flags)
+  __nv_bfloat16 *dk;  // [B,S,Hkv,D]
+  __nv_bfloat16 *dv;  // [B,S,Hkv,D]
+  int B, S, H, Hkv, G, N;
+  int sched, causal;
+  int workers;      // workers per (b, kv head)
+  int total_units;  // B * Hkv * workers
+  float scale_log2; // scale * log2(e)
+  float scale;
+};
+
+struct FwdParams {
+  __nv_bfloat16 *o;  // [B,S,H,D]
+  float *lse;        // [B,H,S]
+  uint32_t *status;
+  int B, S, H, Hkv, G, N;
+  int causal;
+  float scale_log2;
+};
+
+size_t bwd_smem_bytes(int D);
+size_t fwd_smem_bytes(int D);
+
+cudaError_t launch_bwd(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p,
+                       int grid, cudaStream_t stream);
+cudaError_t launch_fwd(int D, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const FwdParams &p, cudaStream_t stream);
+cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
+                              const float *lse, float *dvec, float *lse2, int B, int S, int H,
+                              int D, cudaStream_t stream);
+cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B,
+                              int S, int H, int D, cudaStream_t stream);
+
+}  // namespace dash

@@ -1,0 +1,145 @@
+/*
+ * dash_attn.h -- C ABI of libdash_attn.so: deterministic FlashAttention-style attention
+ * backward (DASH tile schedules) for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation.  Softmax attention O = softmax(scale * Q K^T [masked]) V and its
+ * gradient.  The DASH pages ("DASH: Deterministic Attention Scheduling for
+ * High-throughput Reproducible LLM Training"; gist.science technical summary, section 1
+ * "Problem statement") ask for a backward pass whose gradient accumulation -- dQ in
+ * particular -- happens in a fixed order, so that repeated runs are bit-identical; the
+ * order is given by one of the tile schedules of section 2.2 ("Scheduling strategies").
+ *
+ * Conventions shared by every entry point:
+ *  - Layout BSHD, contiguous, bf16 (IEEE bfloat16 bit patterns):
+ *      Q, O, dO, dQ : [B, S, H,   D]
+ *      K, V, dK, dV : [B, S, Hkv, D]     Hkv = H / group
+ *    LSE: [B, H, S] fp32, natural log of the softmax normaliser of each query row.
+ *  - group = G >= 1 query heads share one K/V head; query head h uses kv head h / G
+ *    (consecutive grouping).  G = 1 is plain multi-head attention.
+ *  - mask: DASH_MASK_FULL, or DASH_MASK_CAUSAL = key j visible to query i iff j <= i
+ *    (top-left aligned; queries and keys have the same length S).
+ *  - scale <= 0 selects 1/sqrt(D).
+ *  - Supported sizes: D in {64, 128}; S a positive multiple of 128; B, H >= 1;
+ *    H % group == 0.  Anything else returns DASH_ERR_UNSUPPORTED (or DASH_ERR_INVALID for
+ *    nonsensical values) synchronously and launches nothing.
+ *  - Pointers: all tensor and workspace pointers are DEVICE pointers owned by the caller
+ *    (for example allocated by PyTorch), 16-byte aligned.  The library allocates no device
+ *    memory, keeps no state between calls other than per-device kernel attributes, and is
+ *    safe to call from several host threads on different streams.
+ *  - Asynchrony: calls enqueue work on `stream` and return; argument errors are reported
+ *    synchronously before anything is enqueued, launch failures as DASH_ERR_CUDA.
+ *  - Device-side failures (a bounded wait that ran out, e.g. an ordering semaphore that
+ *    was never released) do not hang or trap: the kernels record a code in the
+ *    workspace's status word and return.  dash_attn_status() reads it.
+ */
+#ifndef DASH_ATTN_H
+#define DASH_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dash_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
+
+/* Tile schedules (gist.science technical summary, section 2.2).  N = S/128 tiles.
+ *  DASH_SCHED_ATOMIC     -- non-deterministic reference: dQ partials are added with
+ *                           unordered atomics (the "non-deterministic counterpart" of
+ *                           section 1); traversal as SERIAL.
+ *  DASH_SCHED_SERIAL     -- deterministic baseline: the worker owning KV block j visits
+ *                           query tiles in ascending order; every dQ tile adds the KV
+ *                           blocks' partials in ascending kv order.
+ *  DASH_SCHED_DESCENDING -- Descending Q-Tile Iteration (section 2.2 A): traversal
+ *                           reversed (N-1 .. 0), accumulation order unchanged, so dQ is
+ *                           bit-identical to SERIAL.
+ *  DASH_SCHED_SHIFT      -- Shift Scheduling (section 2.2 B).  Full mask: the worker of
+ *                           KV block j visits query tiles j, j+1, .., N-1, 0, .., j-1 and
+ *                           tile q adds KV blocks q, q-1, .., q+1 (mod N).  Causal mask:
+ *                           Symmetric Shift -- the worker c owns KV blocks c and N-1-c,
+ *                           first the dense lower-left rectangle, then the folded
+ *                           triangle; requires an even N. */
+typedef enum {
+  DASH_SCHED_ATOMIC = 0,
+  DASH_SCHED_SERIAL = 1,
+  DASH_SCHED_DESCENDING = 2,
+  DASH_SCHED_SHIFT = 3
+} dash_sched_t;
+
+typedef enum {
+  DASH_OK = 0,
+  DASH_ERR_INVALID = 1,     /* null pointer, non-positive size, misaligned pointer    */
+  DASH_ERR_UNSUPPORTED = 2, /* valid but outside this build's support (D, S, N, GPU)  */
+  DASH_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed            */
+  DASH_ERR_TIMEOUT = 4,     /* a device-side bounded wait ran out (status word set)   */
+  DASH_ERR_WORKSPACE = 5    /* workspace NULL or smaller than required                */
+} dash_status_t;
+
+/* Bytes of device workspace dash_attn_fwd needs (its status word); 0 on bad sizes. */
+size_t dash_attn_fwd_workspace_bytes(int B, int S, int H, int D);
+
+/* Forward pass: O = softmax(scale Q K^T + mask) V and LSE = log of each row's softmax
+ * normaliser (natural log, fp32).  Provides the O and LSE the backward consumes; the
+ * DASH pages take them as given (the method concerns the backward pass only).
+ *   q [B,S,H,D] bf16, k/v [B,S,H/group,D] bf16        (inputs, read only)
+ *   o [B,S,H,D] bf16, lse [B,H,S] fp32                  (outputs, fully overwritten)
+ *   workspace: >= dash_attn_fwd_workspace_bytes(...) bytes of device memory. */
+dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int S, int H, int group, int D, float scale,
+                            dash_mask_t mask, void *workspace, size_t workspace_bytes,
+                            dash_stream_t stream);
+
+/* Bytes of device workspace dash_attn_bwd needs: the fp32 dQ accumulator
+ * (B*H*S*D*4), two fp32 row vectors (B*H*S*4 each), the dQ ordering semaphores
+ * (B*H*(S/128)*4) and a status block; 0 on bad sizes. */
+size_t dash_attn_bwd_workspace_bytes(int B, int S, int H, int D);
+
+/* Backward pass (the DASH hot path): given Q, K, V, O, dO and LSE, writes dQ, dK, dV.
+ *   Steps, all on `stream`: clear the workspace; D_i = rowsum(dO_i * O_i); the tile
+ *   kernel -- per KV block, dK/dV accumulate in tensor memory on one SM while every
+ *   visited query tile's dQ partial is added to an fp32 accumulator in global memory in
+ *   the order the schedule fixes, enforced by one ordering semaphore per dQ tile
+ *   (section 2.1: one KV tile's operations stay on one SM; section 1: fixed dQ
+ *   accumulation order); finally dQ = bf16(scale * accumulator).
+ *   For group > 1, dK/dV of a KV head sum the group's query heads in ascending order.
+ *   Deterministic schedules give bit-identical dQ/dK/dV on every run, for any grid size
+ *   and under concurrent load; DASH_SCHED_ATOMIC does not.
+ *   q, o, dout [B,S,H,D]; k, v [B,S,H/group,D]; lse [B,H,S]    (inputs, read only)
+ *   dq [B,S,H,D]; dk, dv [B,S,H/group,D]                       (outputs, overwritten)
+ *   workspace: >= dash_attn_bwd_workspace_bytes(B,S,H,D) bytes, caller-owned, contents
+ *   need not be initialised; one workspace must not be used by two calls that may run
+ *   concurrently.  Requires S/128 <= number of SMs for DASH_SCHED_SHIFT (all workers of
+ *   a head run concurrently); DASH_SCHED_SHIFT with a causal mask requires S/128 even. */
+dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                            int B, int S, int H, int group, int D, float scale,
+                            dash_mask_t mask, dash_sched_t sched, void *workspace,
+                            size_t workspace_bytes, dash_stream_t stream);
+
+/* Synchronises `stream` and reads the status word of the last call that used
+ * `workspace` (fwd or bwd workspace).  DASH_OK, or DASH_ERR_TIMEOUT when a bounded wait
+ * ran out on the device (the outputs of that call are then undefined). */
+dash_status_t dash_attn_status(void *workspace, dash_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *dash_status_string(dash_status_t status);
+
+/* Host-only view of the tile schedules the backward kernel executes (no GPU needed).
+ * A head has N = S/128 KV blocks and query tiles.  Workers: the per-head units of work
+ * (one KV block, or the pair c, N-1-c for causal DASH_SCHED_SHIFT); each worker runs
+ * one or two segments (one KV block each) of steps; step t of a segment visits query
+ * tile *q with KV block *kv, and its dQ partial is the rank-th addition into tile q.
+ * Return -1 on unsupported arguments. */
+int dash_sched_workers(int sched, int mask, int N);
+int dash_sched_segments(int sched, int mask, int N, int worker);
+int dash_sched_steps(int sched, int mask, int N, int worker, int segment);
+int dash_sched_step(int sched, int mask, int N, int worker, int segment, int step, int *kv,
+                    int *q, int *rank);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DASH_ATTN_H */

@@ -1,0 +1,95 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the header
+declares, rejects bad arguments synchronously, and its schedule tables equal the schedule
+oracle's (host logic only; no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import deterministic_attention_backward_gb300 as dash
+from deterministic_attention_backward_gb300 import _build
+from oracle import schedule as sc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return dash.lib()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "dash_attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dash_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(dash.EXPORTS) == names
+
+
+def test_workspace_sizes(L):
+    B, S, H, D = 2, 1024, 4, 128
+    n = dash.bwd_workspace_bytes(B, S, H, D)
+    rows = B * H * S
+    assert n >= 256 + rows * D * 4 + 2 * rows * 4 + B * H * (S // 128) * 4
+    assert n < 256 + rows * D * 4 + 2 * rows * 4 + B * H * (S // 128) * 4 + 4 * 256
+    assert dash.bwd_workspace_bytes(B, 1000, H, D) == 0          # S not a multiple of 128
+    assert dash.bwd_workspace_bytes(B, S, H, 96) == 0            # unsupported head dim
+    assert dash.fwd_workspace_bytes(B, S, H, 64) == 256
+
+
+def test_argument_errors_are_synchronous(L):
+    null = None
+    c = L.dash_attn_bwd(null, null, null, null, null, null, null, null, null,
+                        1, 512, 2, 1, 64, 0.0, 0, 1, null, 0, null)
+    assert c == 1                                                # DASH_ERR_INVALID
+    c = L.dash_attn_bwd(null, null, null, null, null, null, null, null, null,
+                        1, 500, 2, 1, 64, 0.0, 0, 1, null, 0, null)
+    assert c == 2                                                # S % 128
+    c = L.dash_attn_bwd(null, null, null, null, null, null, null, null, null,
+                        1, 512, 3, 2, 64, 0.0, 0, 1, null, 0, null)
+    assert c == 1                                                # H % group
+    fake = 1 << 20                                               # never dereferenced
+    c = L.dash_attn_bwd(*([fake] * 9), 1, 384, 2, 1, 64, 0.0, 1, 3, fake, 1 << 30, null)
+    assert c == 2                                                # symmetric shift, odd N
+    c = L.dash_attn_bwd(*([fake] * 9), 1, 512, 2, 1, 64, 0.0, 1, 3, fake, 16, null)
+    assert c == 5                                                # workspace too small
+    c = L.dash_attn_bwd(*([fake + 4] + [fake] * 8), 1, 512, 2, 1, 64, 0.0, 1, 3, fake, 1 << 30,
+                        null)
+    assert c == 1                                                # misaligned pointer
+    assert L.dash_status_string(4) == b"device-side wait timed out"
+
+
+SCHEDS = [("serial", sc.SERIAL), ("descending", sc.DESCENDING), ("atomic", sc.SERIAL),
+          ("shift", None)]
+
+
+@pytest.mark.parametrize("N", [2, 4, 6, 8, 16, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("name,oracle_name", SCHEDS)
+def test_library_schedule_equals_oracle(L, name, oracle_name, causal, N):
+    if oracle_name is None:
+        oracle_name = sc.SYMSHIFT if causal else sc.SHIFT
+    table = dash.sched_table(name, causal, N)
+    assert len(table) == sc.num_workers(oracle_name, causal, N)
+    ranks = sc.rank_table(oracle_name, causal, N)
+    for w, segs in enumerate(table):
+        flat = [(kv, q) for seg in segs for kv, q, _ in seg]
+        assert flat == sc.visits(oracle_name, causal, N, w)
+        for seg in segs:
+            assert len({kv for kv, _, _ in seg}) == 1           # one KV block per segment
+            for kv, q, r in seg:
+                assert r == ranks[(q, kv)]
+
+
+def test_schedule_query_rejects_bad_arguments(L):
+    assert L.dash_sched_workers(3, 1, 5) == -1
+    assert L.dash_sched_workers(7, 0, 4) == -1
+    assert L.dash_sched_step(1, 0, 4, 0, 0, 4, None, None, None) == -1
