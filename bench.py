@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Throughput of the deterministic attention backward (DASH schedules) on GB300.
+
+Default workload: full-mask attention backward, H=16, D=128, bf16 N(0,1) inputs,
+B*S = 16384 tokens per batch, one step = one backward pass (prologue + tile kernel + dQ
+convert) for every sequence length of the sweep S in {512, ..., 16384} (B = 16384/S).
+Metric: backward TFLOP/s (algorithmic FLOPs 10*B*H*S^2*D, halved for a causal mask) of the
+deterministic schedule, with the fraction of the measured dense-bf16 peak and the slowdown
+against the non-deterministic atomic-dQ backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--schedule S]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on a bounded sample
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs the same workload on its own
+GPU (independent replicas, no collective on the data path); the value is the sum of the
+ranks' FLOPs over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "deterministic attn-bwd TFLOP/s, % of bf16 tensor peak, slowdown vs atomic-dQ"
+
+WORKLOADS = {
+    "full_h16_d128": dict(
+        desc="full-mask attention backward, H=16, D=128, bf16 N(0,1), B*S=16384, "
+             "S swept over {512,1024,2048,4096,8192,16384}",
+        H=16, Hkv=16, D=128, causal=False, tokens=16384,
+        seqs=[512, 1024, 2048, 4096, 8192, 16384], schedule="shift", ref_S=2048),
+    "causal_h32_d128": dict(
+        desc="causal-mask attention backward, H=32, D=128, bf16 N(0,1), B*S=16384, "
+             "S swept over {1024,2048,4096,8192,16384}",
+        H=32, Hkv=32, D=128, causal=True, tokens=16384,
+        seqs=[1024, 2048, 4096, 8192, 16384], schedule="shift", ref_S=2048),
+    "causal_h32_d64": dict(
+        desc="causal-mask attention backward, H=32, D=64, bf16 N(0,1), B*S=16384, "
+             "S swept over {1024,4096,16384}",
+        H=32, Hkv=32, D=64, causal=True, tokens=16384, seqs=[1024, 4096, 16384],
+        schedule="shift", ref_S=2048),
+    "gqa_causal_8b": dict(
+        desc="GQA causal attention backward shaped like an 8B decoder layer: 32 query heads, "
+             "8 KV heads, D=128, B=2, S=8192",
+        H=32, Hkv=8, D=128, causal=True, tokens=16384, seqs=[8192], schedule="shift",
+        ref_S=2048),
+    "small_b1_h2_s512_d64": dict(
+        desc="full-mask attention backward, B=1, H=2, S=512, D=64 (4 KV blocks)",
+        H=2, Hkv=2, D=64, causal=False, tokens=512, seqs=[512], schedule="shift", ref_S=512),
+}
+SCHEDULES = ["atomic", "serial", "descending", "shift"]
+FALLBACK_PEAK_TFLOPS = 1900.0   # only if the measured-peaks file is absent
+PROFILE = os.path.join(ROOT, "profiles", "bwd_tile_kernel_full_h16_d128.md")
+KERNEL_SOURCES = ["bwd.cu", "ptx.cuh", "sched.cuh", "common.cuh"]
+
+
+def bwd_flops(B, S, H, D, causal):
+    f = 10.0 * B * H * S * S * D
+    return f / 2 if causal else f
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)) or None, "measured"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, None, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "deterministic_attention_backward_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """dram bytes per tile-kernel launch from the committed ncu summary, if it was taken
+    on the current kernel source and this workload; else None."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    src = re.search(r"kernel source sha256\[:16\]:\s*([0-9a-f]+)", text)
+    wl = re.search(r"workload:\s*(\S+)", text)
+    tr = re.search(r"dram bytes per launch \(scaled to the bench launch mix\):\s*([0-9.eE+]+)", text)
+    if not (src and wl and tr) or src.group(1) != kernel_source_hash() or wl.group(1) != workload:
+        return None
+    return float(tr.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.out = index, None, None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.devnull if False else os.path.join(
+                "/tmp", f"dash_clocks_{os.getpid()}.csv"), "w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.proc or not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.seek(0)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        self.out.close()
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def run_gpu(args, wl, rank, world):
+    import torch
+    import deterministic_attention_backward_gb300 as dash
+    from deterministic_attention_backward_gb300 import _build
+    from dash_inputs import make_qkv_do
+
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    sched = args.schedule or wl["schedule"]
+    H, Hkv, D, causal = wl["H"], wl["Hkv"], wl["D"], wl["causal"]
+
+    # inputs resident in HBM, one set per sequence length of the sweep
+    probs = []
+    for S in wl["seqs"]:
+        B = max(1, wl["tokens"] // S)
+        q, k, v, do = (t.to(dev) for t in make_qkv_do(B, S, H, Hkv, D, seed=0))
+        o, lse = dash.fwd(q, k, v, causal=causal, check=True)
+        ws = torch.empty(dash.bwd_workspace_bytes(B, S, H, D), dtype=torch.uint8, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        probs.append(dict(B=B, S=S, q=q, k=k, v=v, do=do, o=o, lse=lse, ws=ws, dq=dq, dk=dk,
+                          dv=dv, flops=bwd_flops(B, S, H, D, causal)))
+    step_flops = sum(p["flops"] for p in probs)
+
+    def call(p, schedule, stages=dash.ALL_STAGES):
+        dash.bwd(p["q"], p["k"], p["v"], p["o"], p["do"], p["lse"], causal=causal,
+                 schedule=schedule, dq=p["dq"], dk=p["dk"], dv=p["dv"], workspace=p["ws"],
+                 stages=stages)
+
+    # correctness guard: the timed schedule must report a clean device status
+    for p in probs:
+        call(p, sched)
+        dash.status(p["ws"])
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps * len(probs))]
+
+    def step(record=None):
+        for j, p in enumerate(probs):
+            call(p, sched, dash.PROLOGUE)
+            if record is not None:
+                evs[record * len(probs) + j][0].record()
+            call(p, sched, dash.TILES)
+            if record is not None:
+                evs[record * len(probs) + j][1].record()
+            call(p, sched, dash.EPILOGUE)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(dev.index) as clk:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        t_start.record()
+        for s in range(args.steps):
+            step(record=s)
+        t_end.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    tile_ms = sum(a.elapsed_time(b) for a, b in evs)
+    for p in probs:
+        dash.status(p["ws"])
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # per-schedule comparison (interleaved, median of reps) on the same inputs
+    reps = max(3, min(10, args.steps))
+    per = {s: [[] for _ in probs] for s in SCHEDULES}
+    for _ in range(reps):
+        for s in SCHEDULES:
+            for j, p in enumerate(probs):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                call(p, s)
+                b.record()
+                per[s][j].append((a, b))
+    torch.cuda.synchronize()
+    sweep = []
+    tot = {s: 0.0 for s in SCHEDULES}
+    for j, p in enumerate(probs):
+        row = {"S": p["S"], "B": p["B"]}
+        for s in SCHEDULES:
+            ms = statistics.median(a.elapsed_time(b) for a, b in per[s][j])
+            tot[s] += ms
+            row[s + "_tflops"] = round(p["flops"] / ms / 1e9, 1)
+        for s in ("serial", "descending", "shift"):
+            row[s + "_slowdown_vs_atomic"] = round(row["atomic_tflops"] / row[s + "_tflops"] - 1, 4)
+        sweep.append(row)
+    sched_summary = {s: round(step_flops / tot[s] / 1e9, 1) for s in SCHEDULES}
+
+    # end to end through the public API with host buffers (pinned), copies in the region
+    e2e_val, h2d, d2h = None, 0, 0
+    if not args.no_e2e:
+        host = []
+        for p in probs:
+            hs = {n: p[n].to("cpu").pin_memory() for n in ("q", "k", "v", "o", "do", "lse")}
+            outs = {n: torch.empty(p[n].shape, dtype=p[n].dtype).pin_memory()
+                    for n in ("dq", "dk", "dv")}
+            host.append((hs, outs))
+            h2d += sum(t.numel() * t.element_size() for t in hs.values())
+            d2h += sum(t.numel() * t.element_size() for t in outs.values())
+
+        def e2e_step():
+            for p, (hs, outs) in zip(probs, host):
+                for n, t in hs.items():
+                    p[n].copy_(t, non_blocking=True)
+                call(p, sched)
+                for n, t in outs.items():
+                    t.copy_(p[n], non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 5))
+        a.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e2e_val = step_flops * n_e2e / (a.elapsed_time(b) / 1e3) / 1e12 * world
+
+    peak, peak_sus, peak_kind = peaks()
+    value = step_flops * args.steps * world / (elapsed_ms / 1e3) / 1e12
+    tile_tflops = step_flops * args.steps / (tile_ms / 1e3) / 1e12
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "description": wl["desc"], "H": H, "Hkv": Hkv,
+                   "D": D, "mask": "causal" if causal else "full", "schedule": sched,
+                   "seq_lens": wl["seqs"], "tokens_per_batch": wl["tokens"],
+                   "l2": "inputs larger than L2 (>= 5 bf16 tensors of 16384x H x D per step "
+                         "point); no flush" if wl["tokens"] * H * D * 2 * 5 > 129e6 else
+                         "inputs smaller than L2; no flush (parity-size workload)",
+                   "step": "prologue + tile kernel + dQ convert for every S of the sweep"},
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "slowdown_vs_atomic": round(sched_summary["atomic"] / sched_summary[sched] - 1, 4),
+        "schedules_tflops": sched_summary,
+        "sweep": sweep,
+        "roofline": {"bound": "tensor", "achieved": round(tile_tflops, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tile_tflops / peak, 4),
+                     "traffic": profiled_traffic(args.workload),
+                     "kernel": "bwd_kernel (tile kernel, " + sched + ")",
+                     "peak_source": f"{peak_kind} dense bf16 burst"
+                                    + (f"; sustained {peak_sus}" if peak_sus else "")},
+        "e2e": {"value": round(e2e_val, 2) if e2e_val else None, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk.summary(),
+        "gpu_launches": 3 * len(probs) * args.steps,
+    }
+    return res
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+class OracleSample:
+    """The fp64 oracle on (batch, kv-head) groups of the workload at S = ref_S, one group
+    per call; the inputs are drawn once."""
+
+    def __init__(self, wl):
+        import oracle
+        from dash_inputs import make_qkv_do
+        self.oracle, self.wl = oracle, wl
+        self.S = wl["ref_S"]
+        self.B = max(1, wl["tokens"] // self.S)
+        self.G = wl["H"] // wl["Hkv"]
+        self.inputs = make_qkv_do(self.B, self.S, wl["H"], wl["Hkv"], wl["D"], seed=0)
+        oracle.build()
+        self.n = 0
+
+    def group(self):
+        """Backward of the next group; returns (algorithmic FLOPs, seconds, threads)."""
+        q, k, v, do = self.inputs
+        b, g = self.n % self.B, (self.n // self.B) % self.wl["Hkv"]
+        self.n += 1
+        hs = slice(g * self.G, (g + 1) * self.G)
+        t0 = time.perf_counter()
+        _, threads = self.oracle.attn_bwd(q[b:b + 1, :, hs], k[b:b + 1, :, g:g + 1],
+                                          v[b:b + 1, :, g:g + 1], do[b:b + 1, :, hs],
+                                          self.wl["causal"], return_threads=True)
+        secs = time.perf_counter() - t0
+        return bwd_flops(1, self.S, self.G, self.wl["D"], self.wl["causal"]), secs, threads
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    smp = OracleSample(wl)
+    flops = secs = 0.0
+    heads = threads = 0
+    while (secs < budget_s or heads == 0) and heads < 64:
+        f, s, threads = smp.group()
+        flops, secs, heads = flops + f, secs + s, heads + 1
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{heads} (batch, kv-head) group(s) at S={smp.S} of this workload, fp64 "
+                      f"C/OpenMP oracle, {secs:.1f} s"}
+
+
+def run_reference(args, wl):
+    smp = OracleSample(wl)
+    for _ in range(args.warmup):
+        smp.group()
+    flops = secs = 0.0
+    threads = 0
+    for _ in range(args.steps):
+        f, s, threads = smp.group()
+        flops, secs = flops + f, secs + s
+    value = flops / secs / 1e12
+    sample = (f"one (batch, kv-head) group at S={smp.S} of this workload per step, "
+              f"fp64 C/OpenMP oracle")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "description": wl["desc"]},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="full_h16_d128", choices=sorted(WORKLOADS))
+    ap.add_argument("--schedule", default=None, choices=SCHEDULES)
+    ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, wl)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, wl, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

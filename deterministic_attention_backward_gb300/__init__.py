@@ -28,7 +28,7 @@ SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "device-side wait timed out", 5: "workspace missing or too small"}
 EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_workspace_bytes",
-           "dash_attn_bwd", "dash_attn_status", "dash_status_string", "dash_sched_workers",
+           "dash_attn_bwd", "dash_attn_bwd_stages", "dash_attn_status", "dash_status_string", "dash_sched_workers",
            "dash_sched_segments", "dash_sched_steps", "dash_sched_step"]
 
 
@@ -63,6 +63,9 @@ def lib() -> ctypes.CDLL:
         L.dash_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i,
                                     vp, sz, vp]
         L.dash_attn_bwd.restype = i
+        L.dash_attn_bwd_stages.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
+                                           i, i, vp, sz, ctypes.c_uint, vp]
+        L.dash_attn_bwd_stages.restype = i
         L.dash_attn_status.argtypes = [vp, vp]
         L.dash_attn_status.restype = i
         L.dash_status_string.argtypes = [i]
@@ -145,11 +148,16 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     return o, l
 
 
+PROLOGUE, TILES, EPILOGUE, ALL_STAGES = 1, 2, 4, 7
+
+
 def bwd(q, k, v, o, do, lse, causal: bool = False, schedule: str = "shift",
         scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None,
-        check: bool = False):
+        check: bool = False, stages: int = ALL_STAGES):
     """Attention backward: returns (dQ, dK, dV) bf16.  ``schedule`` is one of
-    ``atomic`` (non-deterministic reference), ``serial``, ``descending``, ``shift``."""
+    ``atomic`` (non-deterministic reference), ``serial``, ``descending``, ``shift``.
+    ``stages`` (PROLOGUE | TILES | EPILOGUE) launches only part of the work, in order, on
+    the same workspace (for timing the tile kernel on its own)."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
         _require(t, n, torch.bfloat16)
@@ -162,12 +170,13 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, schedule: str = "shift",
     dv = dv if dv is not None else torch.empty_like(v)
     need = bwd_workspace_bytes(B, S, H, D)
     ws = _workspace(need or 256, q.device, workspace)
-    code = lib().dash_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                               do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                               dv.data_ptr(), B, S, H, H // Hkv, D,
-                               float(scale) if scale else 0.0, int(bool(causal)),
-                               SCHEDULES[schedule], ws.data_ptr(),
-                               ws.numel() * ws.element_size(), _stream_ptr(stream))
+    code = lib().dash_attn_bwd_stages(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                                      dk.data_ptr(), dv.data_ptr(), B, S, H, H // Hkv, D,
+                                      float(scale) if scale else 0.0, int(bool(causal)),
+                                      SCHEDULES[schedule], ws.data_ptr(),
+                                      ws.numel() * ws.element_size(), int(stages),
+                                      _stream_ptr(stream))
     _check(code, "dash_attn_bwd")
     if check:
         status(ws, stream)

@@ -167,11 +167,13 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
   return dash::launch_fwd(D, tq, tk, tv, p, s) == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
-dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o,
-                            const void *dout, const float *lse, void *dq, void *dk, void *dv,
-                            int B, int S, int H, int group, int D, float scale,
-                            dash_mask_t mask, dash_sched_t sched, void *workspace,
-                            size_t workspace_bytes, dash_stream_t stream) {
+dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse, void *dq, void *dk,
+                                   void *dv, int B, int S, int H, int group, int D, float scale,
+                                   dash_mask_t mask, dash_sched_t sched, void *workspace,
+                                   size_t workspace_bytes, unsigned stages,
+                                   dash_stream_t stream) {
+  if (stages == 0 || (stages & ~unsigned(DASH_BWD_ALL))) return DASH_ERR_INVALID;
   dash_status_t st = check_sizes(B, S, H, group, D);
   if (st != DASH_OK) return st;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
@@ -202,14 +204,17 @@ dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const v
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const BwdWorkspace w = carve_bwd(workspace, B, S, H, D);
   const float sc = resolve_scale(scale, D);
-  // status word + dQ accumulator are contiguous; semaphores separately
-  if (cudaMemsetAsync(w.status, 0, kStatusBytes + w.dqacc_bytes, s) != cudaSuccess ||
-      cudaMemsetAsync(w.sem, 0, w.sem_bytes, s) != cudaSuccess)
-    return DASH_ERR_CUDA;
-  if (dash::launch_preprocess(static_cast<const __nv_bfloat16 *>(o),
-                              static_cast<const __nv_bfloat16 *>(dout), lse, w.dvec, w.lse2, B, S,
-                              H, D, s) != cudaSuccess)
-    return DASH_ERR_CUDA;
+  if (stages & DASH_BWD_PROLOGUE) {
+    // status word + dQ accumulator are contiguous; semaphores separately
+    if (cudaMemsetAsync(w.status, 0, kStatusBytes + w.dqacc_bytes, s) != cudaSuccess ||
+        cudaMemsetAsync(w.sem, 0, w.sem_bytes, s) != cudaSuccess)
+      return DASH_ERR_CUDA;
+    if (dash::launch_preprocess(static_cast<const __nv_bfloat16 *>(o),
+                                static_cast<const __nv_bfloat16 *>(dout), lse, w.dvec, w.lse2, B,
+                                S, H, D, s) != cudaSuccess)
+      return DASH_ERR_CUDA;
+  }
+  if (!(stages & (DASH_BWD_TILES | DASH_BWD_EPILOGUE))) return DASH_OK;
   dash::BwdParams p{};
   p.lse2 = w.lse2;
   p.dvec = w.dvec;
@@ -230,12 +235,23 @@ dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const v
   p.total_units = (int)total_units;
   p.scale_log2 = sc * dash::kLog2e;
   p.scale = sc;
-  if (dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC, tq, tk, tv, tdo, p, grid, s) != cudaSuccess)
+  if ((stages & DASH_BWD_TILES) &&
+      dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC, tq, tk, tv, tdo, p, grid, s) != cudaSuccess)
     return DASH_ERR_CUDA;
-  if (dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, s) !=
-      cudaSuccess)
+  if ((stages & DASH_BWD_EPILOGUE) &&
+      dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, s) !=
+          cudaSuccess)
     return DASH_ERR_CUDA;
   return DASH_OK;
+}
+
+dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                            int B, int S, int H, int group, int D, float scale,
+                            dash_mask_t mask, dash_sched_t sched, void *workspace,
+                            size_t workspace_bytes, dash_stream_t stream) {
+  return dash_attn_bwd_stages(q, k, v, o, dout, lse, dq, dk, dv, B, S, H, group, D, scale, mask,
+                              sched, workspace, workspace_bytes, DASH_BWD_ALL, stream);
 }
 
 dash_status_t dash_attn_status(void *workspace, dash_stream_t stream) {

@@ -119,6 +119,26 @@ dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const v
                             dash_mask_t mask, dash_sched_t sched, void *workspace,
                             size_t workspace_bytes, dash_stream_t stream);
 
+/* The same backward in separately launchable stages, for callers that time or overlap
+ * them: DASH_BWD_PROLOGUE clears the workspace and computes the row vectors
+ * (rowsum(dO*O), LSE*log2 e); DASH_BWD_TILES runs the tile kernel (the five contractions
+ * and the ordered dQ reduction, dK/dV written); DASH_BWD_EPILOGUE converts the dQ
+ * accumulator to bf16.  Arguments as dash_attn_bwd; stages given in separate calls must
+ * be issued in this order with identical arguments and workspace.  dash_attn_bwd is
+ * dash_attn_bwd_stages(..., DASH_BWD_ALL). */
+typedef enum {
+  DASH_BWD_PROLOGUE = 1,
+  DASH_BWD_TILES = 2,
+  DASH_BWD_EPILOGUE = 4,
+  DASH_BWD_ALL = 7
+} dash_bwd_stage_t;
+dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse, void *dq, void *dk,
+                                   void *dv, int B, int S, int H, int group, int D, float scale,
+                                   dash_mask_t mask, dash_sched_t sched, void *workspace,
+                                   size_t workspace_bytes, unsigned stages,
+                                   dash_stream_t stream);
+
 /* Synchronises `stream` and reads the status word of the last call that used
  * `workspace` (fwd or bwd workspace).  DASH_OK, or DASH_ERR_TIMEOUT when a bounded wait
  * ran out on the device (the outputs of that call are then undefined). */
