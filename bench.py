@@ -170,10 +170,11 @@ def run_gpu(args, wl, rank, world):
     torch.cuda.set_device(dev)
     sched = args.schedule or wl["schedule"]
     H, Hkv, D, causal = wl["H"], wl["Hkv"], wl["D"], wl["causal"]
+    seqs = [args.seq] if args.seq else wl["seqs"]
 
     # inputs resident in HBM, one set per sequence length of the sweep
     probs = []
-    for S in wl["seqs"]:
+    for S in seqs:
         B = max(1, wl["tokens"] // S)
         q, k, v, do = (t.to(dev) for t in make_qkv_do(B, S, H, Hkv, D, seed=0))
         o, lse = dash.fwd(q, k, v, causal=causal, check=True)
@@ -230,6 +231,11 @@ def run_gpu(args, wl, rank, world):
         t = torch.tensor([elapsed_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed_ms = float(t.item())
+
+    if args.quick:  # timed loop only (profiling runs)
+        return {"value_tflops": round(step_flops * args.steps / (elapsed_ms / 1e3) / 1e12, 2),
+                "tile_tflops": round(step_flops * args.steps / (tile_ms / 1e3) / 1e12, 2),
+                "seq_lens": seqs, "schedule": sched, "workload": args.workload}
 
     # per-schedule comparison (interleaved, median of reps) on the same inputs
     reps = max(3, min(10, args.steps))
@@ -298,7 +304,7 @@ def run_gpu(args, wl, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "description": wl["desc"], "H": H, "Hkv": Hkv,
                    "D": D, "mask": "causal" if causal else "full", "schedule": sched,
-                   "seq_lens": wl["seqs"], "tokens_per_batch": wl["tokens"],
+                   "seq_lens": seqs, "tokens_per_batch": wl["tokens"],
                    "l2": "inputs larger than L2 (>= 5 bf16 tensors of 16384x H x D per step "
                          "point); no flush" if wl["tokens"] * H * D * 2 * 5 > 129e6 else
                          "inputs smaller than L2; no flush (parity-size workload)",
@@ -397,6 +403,10 @@ def main():
     ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seq", type=int, default=0,
+                    help="run one sequence length of the workload's sweep only")
+    ap.add_argument("--quick", action="store_true",
+                    help="timed loop only: no schedule table, e2e or CPU baseline (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -415,7 +425,7 @@ def main():
         torch.distributed.init_process_group("nccl")
     res = run_gpu(args, wl, rank, world)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and not args.quick:
             res["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(res), flush=True)
     if world > 1:
