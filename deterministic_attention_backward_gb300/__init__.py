@@ -28,8 +28,9 @@ SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "device-side wait timed out", 5: "workspace missing or too small"}
 EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_workspace_bytes",
-           "dash_attn_bwd", "dash_attn_bwd_stages", "dash_attn_status", "dash_status_string", "dash_sched_workers",
-           "dash_sched_segments", "dash_sched_steps", "dash_sched_step"]
+           "dash_attn_bwd", "dash_attn_bwd_stages", "dash_attn_status",
+           "dash_status_string", "dash_sched_workers", "dash_sched_segments", "dash_sched_steps",
+           "dash_sched_step", "dash_attn_bwd_noalloc"]
 
 
 class DashError(RuntimeError):
@@ -66,6 +67,9 @@ def lib() -> ctypes.CDLL:
         L.dash_attn_bwd_stages.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
                                            i, i, vp, sz, ctypes.c_uint, vp]
         L.dash_attn_bwd_stages.restype = i
+        L.dash_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                            f, i, i, vp]
+        L.dash_attn_bwd_noalloc.restype = i
         L.dash_attn_status.argtypes = [vp, vp]
         L.dash_attn_status.restype = i
         L.dash_status_string.argtypes = [i]

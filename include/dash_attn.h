@@ -144,6 +144,30 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
  * ran out on the device (the outputs of that call are then undefined). */
 dash_status_t dash_attn_status(void *workspace, dash_stream_t stream);
 
+/* Allocation-free backward.  No counterpart on the DASH pages: this is a calling
+ * convenience of this library.  It is for callers that cannot provide a workspace -- for
+ * example a plugin inside an application whose memory pool owns the whole GPU and offers
+ * plugins no allocator, or code where a cudaMalloc would implicitly synchronise the device.
+ * Same arguments and results as dash_attn_bwd, without the workspace: the workspace is a
+ * fixed device array of DASH_NOALLOC_SCRATCH_BYTES inside the library, present on every
+ * GPU that loads the library until the process exits.  The call itself allocates nothing
+ * (no cudaMalloc/cudaFree, no allocating library routine).
+ *   - Limit: sizes whose dash_attn_bwd_workspace_bytes(B,S,H,D) exceeds
+ *     DASH_NOALLOC_SCRATCH_BYTES are rejected with DASH_ERR_WORKSPACE before anything runs
+ *     (64 MiB holds, e.g., B*H*S*(D+2)*4 bytes for B*H*S = 126976 rows at D = 128).
+ *   - The first call on a device (that device current) looks up the array's device address
+ *     with cudaGetSymbolAddress; make that first call before any stream capture.
+ *   - All calls on a device share the array: calls that may overlap on the GPU (e.g. on
+ *     unordered streams) race and corrupt each other's results; order them on one stream.
+ *     Each call re-zeroes the parts that must start at zero.
+ *   - Device-side status (a bounded wait that ran out) is written into the array and cannot
+ *     be read through dash_attn_status; use dash_attn_bwd with a workspace to diagnose. */
+#define DASH_NOALLOC_SCRATCH_BYTES (64u << 20)
+dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                    const void *dout, const float *lse, void *dq, void *dk,
+                                    void *dv, int B, int S, int H, int group, int D, float scale,
+                                    dash_mask_t mask, dash_sched_t sched, dash_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *dash_status_string(dash_status_t status);
 
