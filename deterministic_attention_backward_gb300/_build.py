@@ -45,19 +45,26 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          trace: bool = False) -> str:
+    """Build the library (``trace=True``: the development variant with per-event clocks of
+    CTA 0, written to ``_build/trace/libdash_attn_trace.so``; never the product library)."""
+    out_dir = os.path.join(BUILD, "trace") if trace else BUILD
+    lib = os.path.join(out_dir, "libdash_attn_trace.so") if trace else LIB
+    os.makedirs(out_dir, exist_ok=True)
     deps = _deps()
-    if not force and not _stale(LIB, deps):
-        return LIB
+    if not force and not _stale(lib, deps):
+        return lib
     cc = nvcc()
     common = [cc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-I", INCLUDE, "-I", CSRC]
+    if trace:
+        common += ["-DDASH_TRACE_BUILD"]
     if ptxas_verbose:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         cmd = common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -70,13 +77,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         for _, log in results:
             if log.strip():
                 print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "--cudart", "static", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

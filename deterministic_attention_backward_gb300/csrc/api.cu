@@ -113,6 +113,10 @@ BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
   return w;
 }
 
+#ifdef DASH_TRACE_BUILD
+unsigned long long *g_trace = nullptr;  // development trace build only
+#endif
+
 float resolve_scale(float scale, int D) {
   return scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
 }
@@ -235,6 +239,11 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   p.total_units = (int)total_units;
   p.scale_log2 = sc * dash::kLog2e;
   p.scale = sc;
+#ifdef DASH_TRACE_BUILD
+  p.trace = g_trace;
+#else
+  p.trace = nullptr;
+#endif
   if ((stages & DASH_BWD_TILES) &&
       dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC, tq, tk, tv, tdo, p, grid, s) != cudaSuccess)
     return DASH_ERR_CUDA;
@@ -284,6 +293,11 @@ const char *dash_status_string(dash_status_t s) {
   }
   return "unknown status";
 }
+
+#ifdef DASH_TRACE_BUILD
+// Development trace build only: device buffer of 64 x 32 u64 for CTA 0's event clocks.
+void dash_debug_set_trace(unsigned long long *buf) { g_trace = buf; }
+#endif
 
 // ------------------------------------------------------------------ schedule queries
 static bool sched_args_ok(int sched, int mask, int N) {

@@ -6,7 +6,7 @@
 // operations run back to back on one SM with on-chip accumulation) and visits query
 // tiles in the order of the selected schedule (section 2.2).  Per visited tile (128 query
 // rows i, all in one query head h) it runs the five dense contractions on the tcgen05
-// tensor cores:
+// tensor cores, G3 and G4 split into the two 64-column halves a/b of the query tile:
 //   G1  S^T  = K_j Q_i^T                   (128 x 128 x D)  -> TMEM
 //   G2  dP^T = V_j dO_i^T                  (128 x 128 x D)  -> TMEM
 //       P^T  = exp2(S^T * scale*log2e - LSE_i*log2e)   [causal: 0 above the diagonal]
@@ -21,17 +21,31 @@
 // accumulation order is fixed; the schedules decide which order and how much waiting it
 // costs).  In the atomic mode the additions are unordered.
 //
-// Warp roles (512 threads):
-//   warp 0      TMA producer (one lane): K_j, V_j per segment; Q_i, dO_i, LSE_i, Dvec_i
-//               per step into a ring of shared-memory stages
-//   warp 1      MMA issuer (one lane): G1..G5, tcgen05.commit to mbarriers
+// Pipeline (MMA issue order; every hand-off is an mbarrier):
+//   segment start: G1(first) -> s_full
+//   each step t:   [dQ(t-1) drained] G2(t) -> dp_full,
+//                  [S^T(t) read] G1(t+1) -> s_full        (within the segment)
+//                  [P/dS half a] G3a G4a, [half b] G3b G4b -> stage free,
+//                  G5(t) -> g5_done
+// The softmax-gradient warpgroups read S^T(t) and release its columns at once, so G1(t+1)
+// runs while they compute P and dS; they write P^T and dS^T over the dP^T columns they have
+// just read.  The epilogue copies the dQ partial to registers first and waits for its
+// turn on the semaphore afterwards, so a waiting reduction does not hold tensor memory;
+// each epilogue thread then adds 1 to the semaphore with release semantics after its own
+// reductions, and the next contributor goes when the count reaches 128 x its rank.
+//
+// Warp roles (512 threads; register budgets set per warpgroup with setmaxnreg):
+//   warp 0      TMA producer (converged warp, one elected lane issues): K_j, V_j per
+//               segment; Q_i, dO_i, LSE_i, Dvec_i per step into a ring of stages
+//   warp 1      MMA issuer (converged warp, one elected lane issues): G1..G5 and the
+//               tcgen05.commit arrivals
 //   warp 2      allocates / frees the 512 TMEM columns
 //   warps 4-11  two softmax-gradient warpgroups; warpgroup w handles query columns
 //               [64w, 64w+64) of the tile, thread = KV row (TMEM lane)
 //   warps 12-15 epilogue warpgroup: dQ partial TMEM -> ordered/atomic fp32 reduction in
 //               global memory; dK/dV TMEM -> bf16 at the end of each segment
-// TMEM columns: S^T/P^T [0,128), dP^T/dS^T and the dQ partial [128,256), dK [256,256+D),
-// dV [256+D, 256+2D).
+// TMEM columns: S^T [0,128), dP^T then P^T/dS^T [128,256), dK [256,256+D), dV [256+D,256+2D);
+// the dQ partial reuses [128,256) at D=128 and has its own columns [384,448) at D=64.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -53,14 +67,21 @@ struct BwdLayout {
   static constexpr int offLSE = offDS + kDSBytes;
   static constexpr int offDVEC = offLSE + kStages * kTile * 4;
   static constexpr int offBar = offDVEC + kStages * kTile * 4;
-  static constexpr int kNumBars = 2 * kStages + 9;
+  static constexpr int kNumBars = 2 * kStages + 15;
   static constexpr int offMisc = offBar + kNumBars * 8;
   static constexpr int kBytes = offMisc + 32;
-  static constexpr uint32_t tS = 0, tDP = 128, tDQ = 128, tDK = 256, tDV = 256 + D;
+  static constexpr uint32_t tS = 0, tDP = 128, tDK = 256, tDV = 256 + D;
+  static constexpr uint32_t tDQ = (D == 64) ? 384 : 128;
+  static constexpr bool kDQOwnCols = (D == 64);  // dQ partial does not alias dP^T
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kBytes <= 232448, "shared memory budget");
   static_assert(offDS % 1024 == 0 && offStage % 1024 == 0, "swizzle atoms need 1 KB alignment");
 };
+
+// Register budgets per warpgroup: the launch gives every thread 128 registers
+// (512 x 128 = the SM's 64 K); producer/MMA warpgroup gives some back, the others take them.
+constexpr uint32_t kRegsCtl = 88, kRegsSoftmax = 136, kRegsEpi = 152;
+static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsEpi == 4 * 128, "register split must sum to the launch");
 
 struct Unit {
   int b, hkv, w;
@@ -76,8 +97,8 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams &p, int u) {
 
 template <int D>
 struct Bars {
-  uint64_t *full, *empty, *kv_full, *kv_empty, *sdp_full, *p_ready, *g5_done, *dq_empty,
-      *dkv_full, *dkv_empty, *drain;
+  uint64_t *full, *empty, *kv_full, *kv_empty, *s_full, *s_free, *dp_full, *pds, *g5_done,
+      *dq_empty, *dkv_full, *dkv_empty, *drain;
   __device__ explicit Bars(uint8_t *smem) {
     using L = BwdLayout<D>;
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + L::offBar);
@@ -86,17 +107,20 @@ struct Bars {
     b += 2 * L::kStages;
     kv_full = b + 0;
     kv_empty = b + 1;
-    sdp_full = b + 2;
-    p_ready = b + 3;
-    g5_done = b + 4;
-    dq_empty = b + 5;
-    dkv_full = b + 6;
-    dkv_empty = b + 7;
-    drain = b + 8;
+    s_full = b + 2;   // S^T in TMEM (MMA commit)
+    s_free = b + 3;   // S^T read by both softmax-gradient warpgroups (8 warps)
+    dp_full = b + 4;  // dP^T in TMEM (MMA commit)
+    pds = b + 6;      // [2]: P^T, dS^T of half x in TMEM, dS in shared memory (4 warps)
+    g5_done = b + 10;
+    dq_empty = b + 11;
+    dkv_full = b + 12;
+    dkv_empty = b + 13;
+    drain = b + 14;
   }
 };
 
 // ---------------------------------------------------------------------------------------
+// TMA producer: the whole warp runs the loop; one elected lane issues the copies.
 template <int D>
 __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                              const CUtensorMap *tdo, const BwdParams &p, uint8_t *smem,
@@ -114,17 +138,22 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int kv = seg_kv(p.sched, p.causal, p.N, un.w, seg);
       const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg);
-      if (!mbar_wait(bar.kv_empty, (seg_it & 1) ^ 1, ab)) {
+      if (!mbar_wait_warp(bar.kv_empty, (seg_it & 1) ^ 1, ab)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(bar.kv_full, 2 * L::kTileBytes);
-      const int krow = un.b * p.S + kv * kTile;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar.kv_full, 2 * L::kTileBytes);
+        const int krow = un.b * p.S + kv * kTile;
 #pragma unroll
-      for (int bx = 0; bx < L::kBoxes; ++bx) {
-        tma_load_3d(smem + L::offK + bx * kBoxBytes, tk, bar.kv_full, bx * kBoxCols, un.hkv, krow);
-        tma_load_3d(smem + L::offV + bx * kBoxBytes, tv, bar.kv_full, bx * kBoxCols, un.hkv, krow);
+        for (int bx = 0; bx < L::kBoxes; ++bx) {
+          tma_load_3d(smem + L::offK + bx * kBoxBytes, tk, bar.kv_full, bx * kBoxCols, un.hkv,
+                      krow);
+          tma_load_3d(smem + L::offV + bx * kBoxBytes, tv, bar.kv_full, bx * kBoxCols, un.hkv,
+                      krow);
+        }
       }
+      __syncwarp();
       last_kv = seg_it & 1;
       ++seg_it;
       for (int g = 0; ok && g < p.G; ++g) {
@@ -133,22 +162,25 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
           const int q = step_q(p.sched, p.causal, p.N, un.w, seg, t);
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
-          if (!mbar_wait(&bar.empty[s], ph ^ 1, ab)) {
+          if (!mbar_wait_warp(&bar.empty[s], ph ^ 1, ab)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bar.full[s], L::kStageBytes + 2 * kTile * 4);
-          const int qrow = un.b * p.S + q * kTile;
-          uint8_t *sq = smem + L::offStage + s * L::kStageBytes;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&bar.full[s], L::kStageBytes + 2 * kTile * 4);
+            const int qrow = un.b * p.S + q * kTile;
+            uint8_t *sq = smem + L::offStage + s * L::kStageBytes;
 #pragma unroll
-          for (int bx = 0; bx < L::kBoxes; ++bx) {
-            tma_load_3d(sq + bx * kBoxBytes, tq, &bar.full[s], bx * kBoxCols, h, qrow);
-            tma_load_3d(sq + L::kTileBytes + bx * kBoxBytes, tdo, &bar.full[s], bx * kBoxCols, h,
-                        qrow);
+            for (int bx = 0; bx < L::kBoxes; ++bx) {
+              tma_load_3d(sq + bx * kBoxBytes, tq, &bar.full[s], bx * kBoxCols, h, qrow);
+              tma_load_3d(sq + L::kTileBytes + bx * kBoxBytes, tdo, &bar.full[s], bx * kBoxCols,
+                          h, qrow);
+            }
+            const size_t roff = (size_t)(un.b * p.H + h) * p.S + (size_t)q * kTile;
+            bulk_load(smem + L::offLSE + s * kTile * 4, p.lse2 + roff, kTile * 4, &bar.full[s]);
+            bulk_load(smem + L::offDVEC + s * kTile * 4, p.dvec + roff, kTile * 4, &bar.full[s]);
           }
-          const size_t roff = (size_t)(un.b * p.H + h) * p.S + (size_t)q * kTile;
-          bulk_load(smem + L::offLSE + s * kTile * 4, p.lse2 + roff, kTile * 4, &bar.full[s]);
-          bulk_load(smem + L::offDVEC + s * kTile * 4, p.dvec + roff, kTile * 4, &bar.full[s]);
+          __syncwarp();
           last_full[s] = (int)ph;
           ++it;
         }
@@ -164,14 +196,35 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
 }
 
 // ---------------------------------------------------------------------------------------
+// MMA issuer: the whole warp runs the loop (waits, descriptors and control flow stay
+// warp-uniform); one elected lane issues each tcgen05 instruction.  Within a segment the
+// S^T product of the next step is issued as soon as the softmax-gradient warps have read
+// the current S^T, so it runs while they compute P and dS.
 template <int D>
 __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D> &bar,
                         const Abort &ab) {
   using L = BwdLayout<D>;
   constexpr uint32_t kIdescSS = make_idesc_bf16(128, 128, false, false);  // G1, G2
-  constexpr uint32_t kIdescTS = make_idesc_bf16(128, D, false, true);     // G3, G4
+  constexpr uint32_t kIdescTS = make_idesc_bf16(128, D, false, true);     // G3x, G4x
   constexpr uint32_t kIdescG5 = make_idesc_bf16(128, D, true, true);      // G5
   const uint32_t sbase = smem_u32(smem);
+  // K-major views (contraction over D): k step of 16 columns = +32 B inside a box, boxes
+  // 16 KB apart.  MN-major views (contraction over rows): k step of 16 rows = +2 KB,
+  // 64-column boxes 16 KB apart (the leading-dimension offset).
+  const uint32_t loK = desc_lo(sbase + L::offK, 16), loV = desc_lo(sbase + L::offV, 16);
+  const uint32_t loKmn = desc_lo(sbase + L::offK, kBoxBytes);
+  const uint32_t loDS = desc_lo(sbase + L::offDS, kBoxBytes);
+  auto stage_addr = [&](uint32_t step) { return sbase + L::offStage + (step % L::kStages) * L::kStageBytes; };
+  // G1: S^T = K_j Q_i^T for the step whose Q_i sits in stage (step % kStages)
+  auto issue_g1 = [&](uint32_t step) {
+    const uint32_t loQ = desc_lo(stage_addr(step), 16);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t ko = ((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4;
+      mma_ss_e(tmem + L::tS, desc_of(loK + ko), desc_of(loQ + ko), kIdescSS, k > 0);
+    }
+    mma_commit_e(bar.s_full);
+  };
   uint32_t it = 0, seg_it = 0;
   bool ok = true;
   for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
@@ -179,31 +232,25 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
     const int nseg = sched_segments(p.sched, p.causal);
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg) * p.G;
-      if (!mbar_wait(bar.kv_full, seg_it & 1, ab)) {
+      // segment prologue: new K_j/V_j, the S^T columns free, G1 of the first step
+      if (!mbar_wait_warp(bar.kv_full, seg_it & 1, ab) ||
+          (it > 0 && !mbar_wait_warp(bar.s_free, (it - 1) & 1, ab)) ||
+          !mbar_wait_warp(&bar.full[it % L::kStages], (it / L::kStages) & 1, ab)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      DASH_TRACE(p, 0);
+      issue_g1(it);
       for (int st = 0; st < nsteps; ++st, ++it) {
-        const int s = it % L::kStages;
-        const uint32_t ph = (it / L::kStages) & 1;
-        if (!mbar_wait(&bar.full[s], ph, ab)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t aQ = sbase + L::offStage + s * L::kStageBytes;
-        const uint32_t aDO = aQ + L::kTileBytes;
-        // G1: S^T = K_j Q_i^T  (contraction over D; both operands K-major)
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t koff = (k >> 2) * kBoxBytes + (k & 3) * 32;
-          mma_ss(tmem + L::tS, make_sdesc_sw128(sbase + L::offK + koff, 16, 1024),
-                 make_sdesc_sw128(aQ + koff, 16, 1024), kIdescSS, k > 0);
-        }
-        // the dP^T columns also hold the previous step's dQ partial: wait until drained
-        if (it > 0) {
-          if (!mbar_wait(bar.dq_empty, (it - 1) & 1, ab)) {
+        const uint32_t par = it & 1;
+        const uint32_t aQ = stage_addr(it);
+        const uint32_t loDO = desc_lo(aQ + L::kTileBytes, 16);
+        const uint32_t loQmn = desc_lo(aQ, kBoxBytes);
+        const uint32_t loDOmn = desc_lo(aQ + L::kTileBytes, kBoxBytes);
+        // at D=128 the dP^T columns still hold the previous step's dQ partial
+        if (!L::kDQOwnCols && it > 0) {
+          if (!mbar_wait_warp(bar.dq_empty, (it - 1) & 1, ab)) {
             ok = false;
             break;
           }
@@ -212,71 +259,96 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
         // G2: dP^T = V_j dO_i^T
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t koff = (k >> 2) * kBoxBytes + (k & 3) * 32;
-          mma_ss(tmem + L::tDP, make_sdesc_sw128(sbase + L::offV + koff, 16, 1024),
-                 make_sdesc_sw128(aDO + koff, 16, 1024), kIdescSS, k > 0);
+          const uint32_t ko = ((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4;
+          mma_ss_e(tmem + L::tDP, desc_of(loV + ko), desc_of(loDO + ko), kIdescSS, k > 0);
         }
-        mma_commit(bar.sdp_full);
-        if (!mbar_wait(bar.p_ready, it & 1, ab)) {
-          ok = false;
-          break;
+        mma_commit_e(bar.dp_full);
+        DASH_TRACE(p, 1);
+        // G1 of the next step of this segment, once S^T has been read and Q_{i'} has landed
+        if (st + 1 < nsteps) {
+          if (!mbar_wait_warp(bar.s_free, par, ab) ||
+              !mbar_wait_warp(&bar.full[(it + 1) % L::kStages], ((it + 1) / L::kStages) & 1, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_g1(it + 1);
+          DASH_TRACE(p, 2);
         }
-        tc_fence_after();
-        const bool first = (st == 0);
-        if (first && seg_it > 0) {  // previous segment's dK/dV must have been read out
-          if (!mbar_wait(bar.dkv_empty, (seg_it - 1) & 1, ab)) {
+        const bool fresh = (st == 0);  // first step of a segment starts dK/dV from zero
+        if (fresh && seg_it > 0) {     // previous segment's dK/dV must have been read out
+          if (!mbar_wait_warp(bar.dkv_empty, (seg_it - 1) & 1, ab)) {
             ok = false;
             break;
           }
           tc_fence_after();
         }
-        // G3: dV_j += P^T dO_i ; G4: dK_j += dS^T Q_i  (contraction over the 128 query rows;
-        // A from TMEM, B MN-major).  P^T / dS^T of query columns [64w, 64w+64) sit packed
-        // (bf16x2) in columns [64w, 64w+32) of their region.
+        // G3x: dV_j += P^T dO_i and G4x: dK_j += dS^T Q_i over query half x, once warpgroup x
+        // has put P^T and dS^T of its half into the dP^T columns: within the 32-column chunk
+        // c of the half, P^T packed (bf16x2) in the first 16 columns, dS^T in the next 16.
+#pragma unroll 1
+        for (int x = 0; x < 2; ++x) {
+          if (!mbar_wait_warp(&bar.pds[x], par, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          DASH_TRACE(p, 3 + x);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t pcol = (k < 4) ? 8 * k : 64 + 8 * (k - 4);
-          const uint32_t moff = k * 2048;
-          const uint32_t acc = (first && k == 0) ? 0u : 1u;
-          mma_ts(tmem + L::tDV, tmem + L::tS + pcol,
-                 make_sdesc_sw128(aDO + moff, kBoxBytes, 1024), kIdescTS, acc);
-          mma_ts(tmem + L::tDK, tmem + L::tDP + pcol, make_sdesc_sw128(aQ + moff, kBoxBytes, 1024),
-                 kIdescTS, acc);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t acol = L::tDP + 64 * x + 32 * (k >> 1) + 8 * (k & 1);
+            const uint32_t acc = (fresh && x == 0 && k == 0) ? 0u : 1u;
+            mma_ts_e(tmem + L::tDV, tmem + acol, desc_of(loDOmn + (((4 * x + k) * 2048) >> 4)),
+                     kIdescTS, acc);
+            mma_ts_e(tmem + L::tDK, tmem + acol + 16, desc_of(loQmn + (((4 * x + k) * 2048) >> 4)),
+                     kIdescTS, acc);
+          }
         }
-        mma_commit(&bar.empty[s]);
+        if (!ok) break;
+        mma_commit_e(&bar.empty[it % L::kStages]);
+        if (L::kDQOwnCols && it > 0) {
+          if (!mbar_wait_warp(bar.dq_empty, (it - 1) & 1, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         // G5: dQ_part = dS K_j  (contraction over the 128 KV rows; both operands MN-major)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t moff = k * 2048;
-          mma_ss(tmem + L::tDQ, make_sdesc_sw128(sbase + L::offDS + moff, kBoxBytes, 1024),
-                 make_sdesc_sw128(sbase + L::offK + moff, kBoxBytes, 1024), kIdescG5, k > 0);
-        }
-        mma_commit(bar.g5_done);
+        for (int k = 0; k < 8; ++k)
+          mma_ss_e(tmem + L::tDQ, desc_of(loDS + ((k * 2048) >> 4)),
+                   desc_of(loKmn + ((k * 2048) >> 4)), kIdescG5, k > 0);
+        mma_commit_e(bar.g5_done);
+        DASH_TRACE(p, 5);
         if (st == nsteps - 1) {
-          mma_commit(bar.kv_empty);
-          mma_commit(bar.dkv_full);
+          mma_commit_e(bar.kv_empty);
+          mma_commit_e(bar.dkv_full);
         }
       }
       ++seg_it;
     }
   }
   // leave no MMA in flight
-  mma_commit(bar.drain);
+  mma_commit_e(bar.drain);
   mbar_wait_drain(bar.drain, 0, 100000000ull);
 }
 
 // ---------------------------------------------------------------------------------------
+// Softmax-gradient warpgroup x (query columns [64x, 64x+64) of the tile; thread = KV row):
+// read S^T and release its columns at once, compute P^T in registers, then, when dP^T has
+// arrived, compute dS^T = P^T (dP^T - Dvec) chunk by chunk and write P^T and dS^T (bf16x2)
+// back over the dP^T columns just read; dS also goes to shared memory for G5.
 template <int D>
 __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tmem,
                                  const Bars<D> &bar, const Abort &ab) {
   using L = BwdLayout<D>;
   const int warp = warp_id(), lane = lane_id();
-  const int wg = (warp - 4) >> 2;  // 0 or 1: query columns [64 wg, 64 wg + 64)
+  const int x = (warp - 4) >> 2;  // query half: columns [64x, 64x + 64)
   const int quad = warp & 3;
   const int r = quad * 32 + lane;  // KV row of this thread = TMEM lane
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const int c0 = wg * 64;
-  uint8_t *ds_row = smem + L::offDS + wg * kBoxBytes + r * 128;
+  const int c0 = x * 64;
+  uint8_t *ds_row = smem + L::offDS + x * kBoxBytes + r * 128;
   uint32_t it = 0;
   bool ok = true;
   for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
@@ -291,45 +363,66 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
           const bool diag = p.causal && (q == kv);
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
-          if (!mbar_wait_warp(bar.sdp_full, it & 1, ab) || !mbar_wait_warp(&bar.full[s], ph, ab)) {
+          const uint32_t par = it & 1;
+          if (!mbar_wait_warp(bar.s_full, par, ab) || !mbar_wait_warp(&bar.full[s], ph, ab)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const float *lse_s = reinterpret_cast<const float *>(smem + L::offLSE + s * kTile * 4);
           const float *dvec_s = reinterpret_cast<const float *>(smem + L::offDVEC + s * kTile * 4);
-#pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
-            const int col = c0 + ch * 32;
-            uint32_t sv[32], dpv[32];
-            tmem_ld32(tmem + lane_off + L::tS + col, sv);
-            tmem_ld32(tmem + lane_off + L::tDP + col, dpv);
+          float pf[64];
+          {
+            uint32_t sv[64];
+            tmem_ld32(tmem + lane_off + L::tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tmem_ld32(tmem + lane_off + L::tS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
             tmem_ld_wait();
-            uint32_t pk[16], dk[16];
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar.s_free);  // S^T columns may be overwritten now
+            if (lane == 0 && warp == 4 + 4 * x) DASH_TRACE(p, 6 + 4 * x);
 #pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + col + c);
-              const float4 d4 = *reinterpret_cast<const float4 *>(dvec_s + col + c);
+            for (int c = 0; c < 64; c += 4) {
+              const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + c0 + c);
               const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-              const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-              float pe[4], ds[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float x = fmaf(__uint_as_float(sv[c + e]), p.scale_log2, -lv[e]);
-                float pv = ex2_approx(x);
-                if (diag && (col + c + e) < r) pv = 0.f;
-                pe[e] = pv;
-                ds[e] = pv * (__uint_as_float(dpv[c + e]) - dvv[e]);
+                float pv = ex2_approx(fmaf(__uint_as_float(sv[c + e]), p.scale_log2, -lv[e]));
+                if (diag && (c0 + c + e) < r) pv = 0.f;
+                pf[c + e] = pv;
               }
-              pk[c / 2] = pack_bf16(pe[0], pe[1]);
-              pk[c / 2 + 1] = pack_bf16(pe[2], pe[3]);
+            }
+          }
+          if (lane == 0 && warp == 4 + 4 * x) DASH_TRACE(p, 7 + 4 * x);
+          if (!mbar_wait_warp(bar.dp_full, par, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0 && warp == 4 + 4 * x) DASH_TRACE(p, 8 + 4 * x);
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const uint32_t col = L::tDP + c0 + 32 * ch;
+            uint32_t dpv[32], pk[16], dk[16];
+            tmem_ld32(tmem + lane_off + col, dpv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              const float4 d4 = *reinterpret_cast<const float4 *>(dvec_s + c0 + 32 * ch + c);
+              const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+              float ds[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                ds[e] = pf[32 * ch + c + e] * (__uint_as_float(dpv[c + e]) - dvv[e]);
               dk[c / 2] = pack_bf16(ds[0], ds[1]);
               dk[c / 2 + 1] = pack_bf16(ds[2], ds[3]);
+              pk[c / 2] = pack_bf16(pf[32 * ch + c], pf[32 * ch + c + 1]);
+              pk[c / 2 + 1] = pack_bf16(pf[32 * ch + c + 2], pf[32 * ch + c + 3]);
             }
-            // P^T and dS^T (bf16x2) into the columns this thread has already read
-            tmem_st16(tmem + lane_off + L::tS + c0 + ch * 16, pk);
-            tmem_st16(tmem + lane_off + L::tDP + c0 + ch * 16, dk);
-            // dS into shared memory as the MN-major A operand of G5: row r of box wg,
+            // both into the chunk's own (already read) dP^T columns: P^T, then dS^T
+            tmem_st16(tmem + lane_off + col, pk);
+            tmem_st16(tmem + lane_off + col + 16, dk);
+            // dS into shared memory as the MN-major A operand of G5: row r of box x,
             // 16-byte chunk (4ch + j) at position (4ch + j) ^ (r % 8)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -343,8 +436,9 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(bar.p_ready);
+            mbar_arrive(&bar.pds[x]);
             mbar_arrive(&bar.empty[s]);
+            if (warp == 4 + 4 * x) DASH_TRACE(p, 9 + 4 * x);
           }
         }
       }
@@ -362,9 +456,16 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
   const int quad = warp & 3;
   const int r = quad * 32 + lane;  // query row (dQ) or KV row (dK/dV) = TMEM lane
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  volatile int *decision = reinterpret_cast<volatile int *>(smem + L::offMisc + 8);  // [2]
+  // decisions taken by thread 0 and read by the warpgroup after a named barrier; two
+  // slots alternate so a fast thread 0 never overwrites one that is still being read
+  volatile int *decision = reinterpret_cast<volatile int *>(smem + L::offMisc + 8);
   uint32_t it = 0, seg_it = 0, dec = 0;
   bool ok = true;
+  auto agree = [&](bool mine) -> bool {
+    if (et == 0) decision[dec & 1] = mine ? 1 : 0;
+    named_bar_sync(1, 128);
+    return decision[dec++ & 1] != 0;
+  };
   for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
     const Unit un = decode_unit(p, u);
     const int nseg = sched_segments(p.sched, p.causal);
@@ -378,53 +479,49 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
           int *sem = p.sem + tile_idx;
           const int rank = dq_rank(p.sched, p.causal, p.N, q, kv);
-          if (et == 0) {
-            bool w = mbar_wait(bar.g5_done, it & 1, ab);
-            if (DET && w) w = sem_wait(sem, rank, ab);
-            decision[dec & 1] = w ? 1 : 0;
-          }
-          named_bar_sync(1, 128);
-          if (!decision[dec & 1]) {
+          if (!agree(et == 0 ? mbar_wait(bar.g5_done, it & 1, ab) : true)) {
             ok = false;
             break;
           }
-          ++dec;
           tc_fence_after();
+          if (et == 0) DASH_TRACE(p, 14);
+          // the whole dQ partial row to registers, then give the columns back
+          uint32_t v[D / 32][32];
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tmem + lane_off + L::tDQ + ch * 32, v[ch]);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar.dq_empty);
+          if (et == 0) DASH_TRACE(p, 15);
+          // the semaphore counts the epilogue threads that have finished a partial: the
+          // contributor of rank r goes once all 128 threads of rank r-1 have released
+          if (DET && !agree(et == 0 ? sem_wait(sem, rank * 128, ab) : true)) {
+            ok = false;
+            break;
+          }
+          if (et == 0) DASH_TRACE(p, 16);
           float *tile = p.dqacc + tile_idx * (size_t)(kTile * D);
-#pragma unroll 1
+#pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + L::tDQ + ch * 32, v);
-            tmem_ld_wait();
-            if (ch == D / 32 - 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar.dq_empty);
-            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int c4 = ch * 8 + j;
-              red_add_v4(tile + ((size_t)c4 * kTile + r) * 4, __uint_as_float(v[4 * j]),
-                         __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
-                         __uint_as_float(v[4 * j + 3]));
+              red_add_v4(tile + ((size_t)c4 * kTile + r) * 4, __uint_as_float(v[ch][4 * j]),
+                         __uint_as_float(v[ch][4 * j + 1]), __uint_as_float(v[ch][4 * j + 2]),
+                         __uint_as_float(v[ch][4 * j + 3]));
             }
           }
-          if (DET) {
-            fence_acq_rel_gpu();
-            named_bar_sync(1, 128);
-            if (et == 0) st_release_gpu(sem, rank + 1);
-          }
+          if (DET) red_release_add(sem, 1);  // after this thread's reductions
+          if (et == 0) DASH_TRACE(p, 17);
         }
       }
       if (!ok) break;
       // segment end: dK_j (scaled) and dV_j to bf16
-      if (et == 0) decision[dec & 1] = mbar_wait(bar.dkv_full, seg_it & 1, ab) ? 1 : 0;
-      named_bar_sync(1, 128);
-      if (!decision[dec & 1]) {
+      if (!agree(et == 0 ? mbar_wait(bar.dkv_full, seg_it & 1, ab) : true)) {
         ok = false;
         break;
       }
-      ++dec;
       tc_fence_after();
       const size_t orow = ((size_t)(un.b * p.S + kv * kTile + r) * p.Hkv + un.hkv) * D;
 #pragma unroll 1
@@ -483,8 +580,11 @@ __global__ void __launch_bounds__(512, 1)
     }
     mbar_init(bar.kv_full, 1);
     mbar_init(bar.kv_empty, 1);
-    mbar_init(bar.sdp_full, 1);
-    mbar_init(bar.p_ready, 8);
+    mbar_init(bar.s_full, 1);
+    mbar_init(bar.s_free, 8);
+    mbar_init(bar.dp_full, 1);
+    mbar_init(&bar.pds[0], 4);
+    mbar_init(&bar.pds[1], 4);
     mbar_init(bar.g5_done, 1);
     mbar_init(bar.dq_empty, 4);
     mbar_init(bar.dkv_full, 1);
@@ -508,13 +608,15 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == 0) {
-    if (lane == 0) bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
-  } else if (warp == 1) {
-    if (lane == 0) bwd_mma<D>(p, smem, tmem, bar, ab);
-  } else if (warp >= 4 && warp < 12) {
+  if (warp < 4) {
+    regs_decrease<kRegsCtl>();
+    if (warp == 0) bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
+    if (warp == 1) bwd_mma<D>(p, smem, tmem, bar, ab);
+  } else if (warp < 12) {
+    regs_increase<kRegsSoftmax>();
     bwd_softmax_grad<D>(p, smem, tmem, bar, ab);
-  } else if (warp >= 12) {
+  } else {
+    regs_increase<kRegsEpi>();
     bwd_epilogue<D, DET>(p, smem, tmem, bar, ab);
   }
 
@@ -533,6 +635,11 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   auto kern = bwd_kernel<D, DET>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
+  // the per-warpgroup register split assumes exactly 128 registers per thread at launch
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
   kern<<<grid, 512, L::kBytes, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }

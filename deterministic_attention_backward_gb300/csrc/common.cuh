@@ -37,7 +37,23 @@ struct BwdParams {
   int total_units;  // B * Hkv * workers
   float scale_log2; // scale * log2(e)
   float scale;
+  unsigned long long *trace;  // development trace build only: [64 steps][32 events] clock64
 };
+
+// Development trace build (compiled with -DDASH_TRACE_BUILD into a separate library): the
+// roles of CTA 0 record clock64() at fixed events of their first 64 steps, indexed by the
+// role's own step counter `it`.  In the product build the macro expands to nothing.
+#ifdef DASH_TRACE_BUILD
+#define DASH_TRACE(p, slot)                                              \
+  do {                                                                   \
+    if ((p).trace && blockIdx.x == 0 && it < 64u)                        \
+      (p).trace[it * 32u + (slot)] = (unsigned long long)clock64();      \
+  } while (0)
+#else
+#define DASH_TRACE(p, slot) \
+  do {                      \
+  } while (0)
+#endif
 
 struct FwdParams {
   __nv_bfloat16 *o;  // [B,S,H,D]

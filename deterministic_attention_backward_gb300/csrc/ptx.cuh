@@ -236,6 +236,59 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Elected-lane forms for a converged warp: every lane executes the instruction stream
+// (so loop control and descriptors stay on the warp-uniform datapath) and `elect.sync`
+// lets exactly one lane issue the asynchronous operation.
+__device__ __forceinline__ void mma_ss_e(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_e(uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Descriptor as (constant high word, variable low word): the high word holds the
+// stride-dimension offset 1024 (encoded 64), the version bit and the 128-byte swizzle; the
+// low word holds (address >> 4) | (leading-dimension offset >> 4) << 16.  Advancing along K
+// adds a compile-time constant to the low word only.
+constexpr uint32_t kDescHiSW128 = 64u | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t desc_of(uint32_t lo) {
+  return ((uint64_t)kDescHiSW128 << 32) | lo;
+}
+
 // Arrive once on `bar` when all previously issued tcgen05 async operations of this thread
 // have completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -279,6 +332,19 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 // ----------------------------------------------------------------------------------------
+// Per-warpgroup register budgets (all four warps of a warpgroup execute the same one).
+// The block keeps the registers it was launched with; a warpgroup that lowers its budget
+// returns registers that another warpgroup's increase then takes.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ----------------------------------------------------------------------------------------
 // math and packing
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -310,6 +376,11 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 }
 __device__ __forceinline__ void st_release_gpu(int *p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Add with release semantics at gpu scope: this thread's earlier memory operations (its
+// dQ reductions) are performed before the addition is.
+__device__ __forceinline__ void red_release_add(int *p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
