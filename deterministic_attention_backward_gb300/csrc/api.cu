@@ -194,7 +194,8 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   DevInfo dev;
   if ((st = device_info(&dev)) != DASH_OK) return st;
   const int Hkv = H / group;
-  const int workers = dash::sched_workers(sched, causal, N);
+  const int trav = dash::traversal(sched, causal, N);  // visiting order of the workers
+  const int workers = dash::sched_workers(trav, causal, N);
   const long long total_units = (long long)B * Hkv * workers;
   const int grid = (int)(total_units < dev.sms ? total_units : dev.sms);
   // every worker of a head must be resident at once for the shift schedules
@@ -233,7 +234,7 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   p.Hkv = Hkv;
   p.G = group;
   p.N = N;
-  p.sched = sched;
+  p.sched = trav;
   p.causal = causal;
   p.workers = workers;
   p.total_units = (int)total_units;
@@ -307,30 +308,33 @@ static bool sched_args_ok(int sched, int mask, int N) {
 }
 
 int dash_sched_workers(int sched, int mask, int N) {
-  return sched_args_ok(sched, mask, N) ? dash::sched_workers(sched, mask, N) : -1;
+  if (!sched_args_ok(sched, mask, N)) return -1;
+  return dash::sched_workers(dash::traversal(sched, mask, N), mask, N);
 }
 
 int dash_sched_segments(int sched, int mask, int N, int worker) {
-  if (!sched_args_ok(sched, mask, N) || worker < 0 || worker >= dash::sched_workers(sched, mask, N))
-    return -1;
-  return dash::sched_segments(sched, mask);
+  const int W = dash_sched_workers(sched, mask, N);
+  if (W < 0 || worker < 0 || worker >= W) return -1;
+  return dash::sched_segments(dash::traversal(sched, mask, N), mask);
 }
 
 int dash_sched_steps(int sched, int mask, int N, int worker, int segment) {
   const int nseg = dash_sched_segments(sched, mask, N, worker);
   if (nseg < 0 || segment < 0 || segment >= nseg) return -1;
-  return dash::seg_steps(sched, mask, N, worker, segment);
+  return dash::seg_steps(dash::traversal(sched, mask, N), mask, N, worker, segment);
 }
 
 int dash_sched_step(int sched, int mask, int N, int worker, int segment, int step, int *kv,
                     int *q, int *rank) {
   const int n = dash_sched_steps(sched, mask, N, worker, segment);
   if (n < 0 || step < 0 || step >= n) return -1;
-  const int kvb = dash::seg_kv(sched, mask, N, worker, segment);
-  const int qt = dash::step_q(sched, mask, N, worker, segment, step);
+  const int t = dash::traversal(sched, mask, N);
+  const int kvb = dash::seg_kv(t, mask, N, worker, segment);
+  const int qt = dash::step_q(t, mask, N, worker, segment, step);
   if (kv) *kv = kvb;
   if (q) *q = qt;
-  if (rank) *rank = dash::dq_rank(sched, mask, N, qt, kvb);
+  // ATOMIC adds in no fixed order; report the position the traversal would give
+  if (rank) *rank = dash::dq_rank(t, mask, N, qt, kvb);
   return 0;
 }
 

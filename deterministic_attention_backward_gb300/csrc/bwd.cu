@@ -80,8 +80,15 @@ struct BwdLayout {
 
 // Register budgets per warpgroup: the launch gives every thread 128 registers
 // (512 x 128 = the SM's 64 K); producer/MMA warpgroup gives some back, the others take them.
-constexpr uint32_t kRegsCtl = 88, kRegsSoftmax = 136, kRegsEpi = 152;
-static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsEpi == 4 * 128, "register split must sum to the launch");
+// At D=64 the epilogue holds only 64 dQ values, so the softmax-gradient warpgroups get more.
+template <int D>
+struct RegSplit {
+  static constexpr uint32_t kLaunch = 128;  // 65536 registers / 512 threads
+  static constexpr uint32_t kCtl = 88;
+  static constexpr uint32_t kSoftmax = (D == 64) ? 152 : 136;
+  static constexpr uint32_t kEpi = (D == 64) ? 120 : 152;
+  static_assert(kCtl + 2 * kSoftmax + kEpi == 4 * kLaunch, "register split must sum to the launch");
+};
 
 struct Unit {
   int b, hkv, w;
@@ -609,14 +616,14 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t tmem = *s_tmem;
 
   if (warp < 4) {
-    regs_decrease<kRegsCtl>();
+    regs_set<RegSplit<D>::kCtl, RegSplit<D>::kLaunch>();
     if (warp == 0) bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
     if (warp == 1) bwd_mma<D>(p, smem, tmem, bar, ab);
   } else if (warp < 12) {
-    regs_increase<kRegsSoftmax>();
+    regs_set<RegSplit<D>::kSoftmax, RegSplit<D>::kLaunch>();
     bwd_softmax_grad<D>(p, smem, tmem, bar, ab);
   } else {
-    regs_increase<kRegsEpi>();
+    regs_set<RegSplit<D>::kEpi, RegSplit<D>::kLaunch>();
     bwd_epilogue<D, DET>(p, smem, tmem, bar, ab);
   }
 
@@ -639,7 +646,7 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
+  if (fa.numRegs != (int)RegSplit<D>::kLaunch) return cudaErrorInvalidConfiguration;
   kern<<<grid, 512, L::kBytes, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }

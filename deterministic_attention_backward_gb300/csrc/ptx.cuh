@@ -343,6 +343,18 @@ template <uint32_t N>
 __device__ __forceinline__ void regs_decrease() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
+// Move this warpgroup from the launch budget `kLaunch` to `N` registers per thread: an
+// increase for N above it, a decrease below it (setmaxnreg.inc may only raise the budget and
+// .dec only lower it).
+template <uint32_t N, uint32_t kLaunch>
+__device__ __forceinline__ void regs_set() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg budget");
+  if constexpr (N > kLaunch) {
+    regs_increase<N>();
+  } else if constexpr (N < kLaunch) {
+    regs_decrease<N>();
+  }
+}
 
 // ----------------------------------------------------------------------------------------
 // math and packing

@@ -25,7 +25,10 @@
 //      q <  h            : rank = q - kv
 //      q >= h, kv <  h   : rank = (q - h - kv) mod h
 //      q >= h, kv >= h   : rank = kv       (= h + (kv - h), after the h rectangle ones)
-//  ATOMIC: SERIAL traversal, no order.
+//  ATOMIC: no order; it visits tiles in the shift order (conflict-free and, for the causal
+//    mask, balanced), the most favourable traversal, so that the deterministic schedules
+//    are compared against the fastest non-deterministic backward; odd-N causal falls back
+//    to the SERIAL traversal.
 #pragma once
 
 #if defined(__CUDACC__)
@@ -37,6 +40,12 @@
 namespace dash {
 
 enum Sched : int { kAtomic = 0, kSerial = 1, kDescending = 2, kShift = 3 };
+
+// Which visiting order a schedule uses (ATOMIC borrows the shift order when it exists).
+DASH_HD int traversal(int sched, int causal, int N) {
+  if (sched != kAtomic) return sched;
+  return (!causal || (N % 2) == 0) ? kShift : kSerial;
+}
 
 DASH_HD bool sym_shift(int sched, int causal) { return sched == kShift && causal; }
 

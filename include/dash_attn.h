@@ -49,7 +49,10 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
 /* Tile schedules (gist.science technical summary, section 2.2).  N = S/128 tiles.
  *  DASH_SCHED_ATOMIC     -- non-deterministic reference: dQ partials are added with
  *                           unordered atomics (the "non-deterministic counterpart" of
- *                           section 1); traversal as SERIAL.
+ *                           section 1).  It visits tiles in the SHIFT order (cyclic /
+ *                           symmetric; SERIAL for a causal mask with odd N), the fastest
+ *                           traversal, so that it is the speed reference for the
+ *                           deterministic schedules.
  *  DASH_SCHED_SERIAL     -- deterministic baseline: the worker owning KV block j visits
  *                           query tiles in ascending order; every dQ tile adds the KV
  *                           blocks' partials in ascending kv order.

@@ -67,7 +67,7 @@ def test_argument_errors_are_synchronous(L):
     assert L.dash_status_string(4) == b"device-side wait timed out"
 
 
-SCHEDS = [("serial", sc.SERIAL), ("descending", sc.DESCENDING), ("atomic", sc.SERIAL),
+SCHEDS = [("serial", sc.SERIAL), ("descending", sc.DESCENDING), ("atomic", None),
           ("shift", None)]
 
 
@@ -75,7 +75,7 @@ SCHEDS = [("serial", sc.SERIAL), ("descending", sc.DESCENDING), ("atomic", sc.SE
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("name,oracle_name", SCHEDS)
 def test_library_schedule_equals_oracle(L, name, oracle_name, causal, N):
-    if oracle_name is None:
+    if oracle_name is None:  # shift; the atomic reference borrows the shift traversal
         oracle_name = sc.SYMSHIFT if causal else sc.SHIFT
     table = dash.sched_table(name, causal, N)
     assert len(table) == sc.num_workers(oracle_name, causal, N)
@@ -87,6 +87,12 @@ def test_library_schedule_equals_oracle(L, name, oracle_name, causal, N):
             assert len({kv for kv, _, _ in seg}) == 1           # one KV block per segment
             for kv, q, r in seg:
                 assert r == ranks[(q, kv)]
+
+
+def test_atomic_odd_causal_falls_back_to_serial_traversal(L):
+    table = dash.sched_table("atomic", True, 5)
+    flat = [[(kv, q) for seg in segs for kv, q, _ in seg] for segs in table]
+    assert flat == [sc.visits(sc.SERIAL, True, 5, w) for w in range(5)]
 
 
 def test_schedule_query_rejects_bad_arguments(L):
