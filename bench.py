@@ -39,17 +39,17 @@ WORKLOADS = {
         desc="full-mask attention backward, H=16, D=128, bf16 N(0,1), B*S=16384, "
              "S swept over {512,1024,2048,4096,8192,16384}",
         H=16, Hkv=16, D=128, causal=False, tokens=16384,
-        seqs=[512, 1024, 2048, 4096, 8192, 16384], schedule="shift", ref_S=2048),
+        seqs=[512, 1024, 2048, 4096, 8192, 16384], schedule="shift_fill", ref_S=2048),
     "causal_h32_d128": dict(
         desc="causal-mask attention backward, H=32, D=128, bf16 N(0,1), B*S=16384, "
              "S swept over {1024,2048,4096,8192,16384}",
         H=32, Hkv=32, D=128, causal=True, tokens=16384,
-        seqs=[1024, 2048, 4096, 8192, 16384], schedule="shift", ref_S=2048),
+        seqs=[1024, 2048, 4096, 8192, 16384], schedule="shift_fill", ref_S=2048),
     "causal_h32_d64": dict(
         desc="causal-mask attention backward, H=32, D=64, bf16 N(0,1), B*S=16384, "
              "S swept over {1024,4096,16384}",
         H=32, Hkv=32, D=64, causal=True, tokens=16384, seqs=[1024, 4096, 16384],
-        schedule="shift", ref_S=2048),
+        schedule="shift_fill", ref_S=2048),
     "gqa_causal_8b": dict(
         desc="GQA causal attention backward shaped like an 8B decoder layer: 32 query heads, "
              "8 KV heads, D=128, B=2, S=8192",
@@ -57,9 +57,10 @@ WORKLOADS = {
         ref_S=2048),
     "small_b1_h2_s512_d64": dict(
         desc="full-mask attention backward, B=1, H=2, S=512, D=64 (4 KV blocks)",
-        H=2, Hkv=2, D=64, causal=False, tokens=512, seqs=[512], schedule="shift", ref_S=512),
+        H=2, Hkv=2, D=64, causal=False, tokens=512, seqs=[512], schedule="shift_fill", ref_S=512),
 }
-SCHEDULES = ["atomic", "serial", "descending", "shift"]
+SCHEDULES = ["atomic", "serial", "descending", "shift", "shift_fill"]
+DETERMINISTIC = ["serial", "descending", "shift", "shift_fill"]
 FALLBACK_PEAK_TFLOPS = 1900.0   # only if the measured-peaks file is absent
 PROFILE = os.path.join(ROOT, "profiles", "bwd_tile_kernel_full_h16_d128.md")
 KERNEL_SOURCES = ["bwd.cu", "ptx.cuh", "sched.cuh", "common.cuh"]
@@ -257,7 +258,7 @@ def run_gpu(args, wl, rank, world):
             ms = statistics.median(a.elapsed_time(b) for a, b in per[s][j])
             tot[s] += ms
             row[s + "_tflops"] = round(p["flops"] / ms / 1e9, 1)
-        for s in ("serial", "descending", "shift"):
+        for s in DETERMINISTIC:
             row[s + "_slowdown_vs_atomic"] = round(row["atomic_tflops"] / row[s + "_tflops"] - 1, 4)
         sweep.append(row)
     sched_summary = {s: round(step_flops / tot[s] / 1e9, 1) for s in SCHEDULES}

@@ -19,18 +19,18 @@ import os
 import threading
 
 __all__ = ["fwd", "bwd", "bwd_workspace_bytes", "fwd_workspace_bytes", "status",
-           "sched_table", "SCHEDULES", "lib", "DashError"]
+           "sched_table", "sched_plan", "SCHEDULES", "lib", "DashError"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdash_attn.so")
 
-SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3}
+SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3, "shift_fill": 4}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "device-side wait timed out", 5: "workspace missing or too small"}
 EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_workspace_bytes",
            "dash_attn_bwd", "dash_attn_bwd_stages", "dash_attn_status",
            "dash_status_string", "dash_sched_workers", "dash_sched_segments", "dash_sched_steps",
-           "dash_sched_step", "dash_attn_bwd_noalloc"]
+           "dash_sched_step", "dash_sched_plan", "dash_attn_bwd_noalloc"]
 
 
 class DashError(RuntimeError):
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.dash_sched_steps.restype = i
         L.dash_sched_step.argtypes = [i, i, i, i, i, i, ip, ip, ip]
         L.dash_sched_step.restype = i
+        L.dash_sched_plan.argtypes = [i, i, i, i, i, ip, ip, ip]
+        L.dash_sched_plan.restype = i
         _lib = L
         return L
 
@@ -159,7 +161,8 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, schedule: str = "shift",
         scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None,
         check: bool = False, stages: int = ALL_STAGES):
     """Attention backward: returns (dQ, dK, dV) bf16.  ``schedule`` is one of
-    ``atomic`` (non-deterministic reference), ``serial``, ``descending``, ``shift``.
+    ``atomic`` (non-deterministic reference), ``serial``, ``descending``, ``shift``,
+    ``shift_fill`` (shift on whole heads, descending on the SMs left over).
     ``stages`` (PROLOGUE | TILES | EPILOGUE) launches only part of the work, in order, on
     the same workspace (for timing the tile kernel on its own)."""
     import torch
@@ -191,6 +194,17 @@ def status(workspace, stream=None):
     """Synchronise and raise DashError if the last call on ``workspace`` reported a
     device-side failure (a bounded wait that ran out)."""
     _check(lib().dash_attn_status(workspace.data_ptr(), _stream_ptr(stream)), "device status")
+
+
+def sched_plan(schedule: str, causal: bool, N: int, heads: int, sms: int):
+    """(heads on the requested schedule, SMs they use, total CTAs) for ``heads`` (batch,
+    kv-head) pairs on a GPU with ``sms`` SMs; the rest run DESCENDING (fill mode only)."""
+    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    code = lib().dash_sched_plan(SCHEDULES[schedule], int(bool(causal)), N, heads, sms,
+                                 ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    if code != 0:
+        raise ValueError("unsupported schedule arguments")
+    return a.value, b.value, c.value
 
 
 def sched_table(schedule: str, causal: bool, N: int):

@@ -117,6 +117,57 @@ BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
 unsigned long long *g_trace = nullptr;  // development trace build only
 #endif
 
+// How the backward tile kernel's grid is used: heads [0, heads_a) run schedule sched_a on
+// CTAs [0, grid_a), the remaining heads run sched_b on CTAs [grid_a, grid).
+struct LaunchPlan {
+  int sched_a, workers_a, heads_a, grid_a, sched_b, workers_b, grid;
+};
+
+// False when a shift schedule cannot have every worker of a head resident at once.
+bool make_plan(int sched, int causal, int N, int heads, int sms, LaunchPlan *pl) {
+  const int trav = dash::traversal(sched, causal, N);
+  const int W = dash::sched_workers(trav, causal, N);
+  const long long total = (long long)heads * W;
+  pl->sched_a = pl->sched_b = trav;
+  pl->workers_a = pl->workers_b = W;
+  pl->heads_a = heads;
+  pl->grid = pl->grid_a = (int)(total < sms ? total : sms);
+  const bool shift = sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL;
+  if (shift && W > sms) return false;
+  if (sched != DASH_SCHED_SHIFT_FILL) return true;
+  const int k = sms / W;  // whole heads per round of the shift group
+  if (heads <= k) return true;
+  const int grid_a = k * W, L = sms - grid_a;
+  if (L == 0) return true;
+  // Group B runs DESCENDING (no co-residency needed) on the L leftover SMs.  Its head count
+  // balances the estimated finish times; tile steps per SM of DESCENDING are taken as 0.7
+  // of the shift schedule's (it pays the serialized pipeline fill of each head).
+  const double unit_a = causal ? N + 1.0 : (double)N;              // steps of a shift worker
+  const double head_work = causal ? N * (N + 1) / 2.0 : (double)N * N;  // tile steps per head
+  const double eff_b = 0.7;
+  int best_hb = 0;
+  double best = std::ceil((double)heads / k) * unit_a;
+  for (int hb = 1; hb < heads; ++hb) {
+    const double ta = std::ceil((double)(heads - hb) / k) * unit_a;
+    const double tb = hb * head_work / (L * eff_b);
+    const double t = ta > tb ? ta : tb;
+    if (t < best) {
+      best = t;
+      best_hb = hb;
+    }
+  }
+  pl->grid_a = grid_a;
+  if (best_hb == 0) {  // whole-head rounds only, the leftover SMs stay idle
+    pl->grid = grid_a;
+    return true;
+  }
+  pl->heads_a = heads - best_hb;
+  pl->grid = sms;
+  pl->sched_b = dash::kDescending;
+  pl->workers_b = N;
+  return true;
+}
+
 float resolve_scale(float scale, int D) {
   return scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
 }
@@ -181,25 +232,23 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   dash_status_t st = check_sizes(B, S, H, group, D);
   if (st != DASH_OK) return st;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
-  if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_SHIFT) return DASH_ERR_INVALID;
+  if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_SHIFT_FILL) return DASH_ERR_INVALID;
   const void *ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
   for (const void *ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return DASH_ERR_INVALID;
   const int N = S / kTile;
   const int causal = mask == DASH_MASK_CAUSAL;
-  if (sched == DASH_SCHED_SHIFT && causal && (N % 2)) return DASH_ERR_UNSUPPORTED;
+  const bool shift = sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL;
+  if (shift && causal && (N % 2)) return DASH_ERR_UNSUPPORTED;
   const BwdWorkspace need = carve_bwd(nullptr, B, S, H, D);
   if (!workspace || !aligned16(workspace) || workspace_bytes < need.total)
     return DASH_ERR_WORKSPACE;
   DevInfo dev;
   if ((st = device_info(&dev)) != DASH_OK) return st;
   const int Hkv = H / group;
-  const int trav = dash::traversal(sched, causal, N);  // visiting order of the workers
-  const int workers = dash::sched_workers(trav, causal, N);
-  const long long total_units = (long long)B * Hkv * workers;
-  const int grid = (int)(total_units < dev.sms ? total_units : dev.sms);
+  LaunchPlan plan;
   // every worker of a head must be resident at once for the shift schedules
-  if (sched == DASH_SCHED_SHIFT && workers > grid) return DASH_ERR_UNSUPPORTED;
+  if (!make_plan(sched, causal, N, B * Hkv, dev.sms, &plan)) return DASH_ERR_UNSUPPORTED;
 
   CUtensorMap tq, tk, tv, tdo;
   if (!make_bshd_map(&tq, q, B, S, H, D) || !make_bshd_map(&tk, k, B, S, Hkv, D) ||
@@ -234,10 +283,14 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   p.Hkv = Hkv;
   p.G = group;
   p.N = N;
-  p.sched = trav;
   p.causal = causal;
-  p.workers = workers;
-  p.total_units = (int)total_units;
+  p.heads = B * Hkv;
+  p.sched_a = plan.sched_a;
+  p.workers_a = plan.workers_a;
+  p.heads_a = plan.heads_a;
+  p.grid_a = plan.grid_a;
+  p.sched_b = plan.sched_b;
+  p.workers_b = plan.workers_b;
   p.scale_log2 = sc * dash::kLog2e;
   p.scale = sc;
 #ifdef DASH_TRACE_BUILD
@@ -246,7 +299,8 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   p.trace = nullptr;
 #endif
   if ((stages & DASH_BWD_TILES) &&
-      dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC, tq, tk, tv, tdo, p, grid, s) != cudaSuccess)
+      dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC, tq, tk, tv, tdo, p, plan.grid, s) !=
+          cudaSuccess)
     return DASH_ERR_CUDA;
   if ((stages & DASH_BWD_EPILOGUE) &&
       dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, s) !=
@@ -302,9 +356,22 @@ void dash_debug_set_trace(unsigned long long *buf) { g_trace = buf; }
 
 // ------------------------------------------------------------------ schedule queries
 static bool sched_args_ok(int sched, int mask, int N) {
-  if (sched < 0 || sched > 3 || (mask != 0 && mask != 1) || N <= 0) return false;
-  if (sched == DASH_SCHED_SHIFT && mask == 1 && (N % 2)) return false;
+  if (sched < 0 || sched > 4 || (mask != 0 && mask != 1) || N <= 0) return false;
+  if ((sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL) && mask == 1 && (N % 2))
+    return false;
   return true;
+}
+
+int dash_sched_plan(int sched, int mask, int N, int heads, int sms, int *heads_a, int *sms_a,
+                    int *grid) {
+  LaunchPlan pl;
+  if (!sched_args_ok(sched, mask, N) || heads <= 0 || sms <= 0 ||
+      !make_plan(sched, mask, N, heads, sms, &pl))
+    return -1;
+  if (heads_a) *heads_a = pl.heads_a;
+  if (sms_a) *sms_a = pl.grid_a;
+  if (grid) *grid = pl.grid;
+  return 0;
 }
 
 int dash_sched_workers(int sched, int mask, int N) {

@@ -90,15 +90,34 @@ struct RegSplit {
   static_assert(kCtl + 2 * kSoftmax + kEpi == 4 * kLaunch, "register split must sum to the launch");
 };
 
+// Work of this CTA.  The heads are split into two groups with their own schedule and their
+// own CTAs (the split is a single group unless the fill mode is used): group A are heads
+// [0, heads_a) on CTAs [0, grid_a), group B the remaining heads on the remaining CTAs.
+// Within a group, worker u of the group runs on CTA (u mod group size), in order.
+struct Plan {
+  int sched, W, first, stride, nunits, head_off;
+};
+__device__ __forceinline__ Plan cta_plan(const BwdParams &p) {
+  Plan pl;
+  const bool grp_b = (int)blockIdx.x >= p.grid_a;
+  pl.sched = grp_b ? p.sched_b : p.sched_a;
+  pl.W = grp_b ? p.workers_b : p.workers_a;
+  pl.first = grp_b ? (int)blockIdx.x - p.grid_a : (int)blockIdx.x;
+  pl.stride = grp_b ? (int)gridDim.x - p.grid_a : p.grid_a;
+  pl.nunits = (grp_b ? p.heads - p.heads_a : p.heads_a) * pl.W;
+  pl.head_off = grp_b ? p.heads_a : 0;
+  return pl;
+}
+
 struct Unit {
   int b, hkv, w;
 };
-__device__ __forceinline__ Unit decode_unit(const BwdParams &p, int u) {
+__device__ __forceinline__ Unit decode_unit(const BwdParams &p, const Plan &pl, int u) {
   Unit r;
-  r.w = u % p.workers;
-  const int bh = u / p.workers;
-  r.hkv = bh % p.Hkv;
-  r.b = bh / p.Hkv;
+  r.w = u % pl.W;
+  const int hd = pl.head_off + u / pl.W;  // head index b * Hkv + hkv
+  r.hkv = hd % p.Hkv;
+  r.b = hd / p.Hkv;
   return r;
 }
 
@@ -139,12 +158,13 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
   for (int s = 0; s < L::kStages; ++s) last_full[s] = -1;
   int last_kv = -1;
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-    const Unit un = decode_unit(p, u);
-    const int nseg = sched_segments(p.sched, p.causal);
+  const Plan pl = cta_plan(p);
+  for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
+    const Unit un = decode_unit(p, pl, u);
+    const int nseg = sched_segments(pl.sched, p.causal);
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(p.sched, p.causal, p.N, un.w, seg);
-      const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg);
+      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
       if (!mbar_wait_warp(bar.kv_empty, (seg_it & 1) ^ 1, ab)) {
         ok = false;
         break;
@@ -166,7 +186,7 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
       for (int g = 0; ok && g < p.G; ++g) {
         const int h = un.hkv * p.G + g;
         for (int t = 0; t < nsteps; ++t) {
-          const int q = step_q(p.sched, p.causal, p.N, un.w, seg, t);
+          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
           if (!mbar_wait_warp(&bar.empty[s], ph ^ 1, ab)) {
@@ -234,11 +254,12 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
   };
   uint32_t it = 0, seg_it = 0;
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-    const Unit un = decode_unit(p, u);
-    const int nseg = sched_segments(p.sched, p.causal);
+  const Plan pl = cta_plan(p);
+  for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
+    const Unit un = decode_unit(p, pl, u);
+    const int nseg = sched_segments(pl.sched, p.causal);
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg) * p.G;
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg) * p.G;
       // segment prologue: new K_j/V_j, the S^T columns free, G1 of the first step
       if (!mbar_wait_warp(bar.kv_full, seg_it & 1, ab) ||
           (it > 0 && !mbar_wait_warp(bar.s_free, (it - 1) & 1, ab)) ||
@@ -358,15 +379,16 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
   uint8_t *ds_row = smem + L::offDS + x * kBoxBytes + r * 128;
   uint32_t it = 0;
   bool ok = true;
-  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-    const Unit un = decode_unit(p, u);
-    const int nseg = sched_segments(p.sched, p.causal);
+  const Plan pl = cta_plan(p);
+  for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
+    const Unit un = decode_unit(p, pl, u);
+    const int nseg = sched_segments(pl.sched, p.causal);
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(p.sched, p.causal, p.N, un.w, seg);
-      const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg);
+      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
       for (int g = 0; ok && g < p.G; ++g) {
         for (int t = 0; t < nsteps; ++t, ++it) {
-          const int q = step_q(p.sched, p.causal, p.N, un.w, seg, t);
+          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
           const bool diag = p.causal && (q == kv);
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
@@ -473,19 +495,20 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
     named_bar_sync(1, 128);
     return decision[dec++ & 1] != 0;
   };
-  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-    const Unit un = decode_unit(p, u);
-    const int nseg = sched_segments(p.sched, p.causal);
+  const Plan pl = cta_plan(p);
+  for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
+    const Unit un = decode_unit(p, pl, u);
+    const int nseg = sched_segments(pl.sched, p.causal);
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(p.sched, p.causal, p.N, un.w, seg);
-      const int nsteps = seg_steps(p.sched, p.causal, p.N, un.w, seg);
+      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
       for (int g = 0; ok && g < p.G; ++g) {
         const int h = un.hkv * p.G + g;
         for (int t = 0; t < nsteps; ++t, ++it) {
-          const int q = step_q(p.sched, p.causal, p.N, un.w, seg, t);
+          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
           int *sem = p.sem + tile_idx;
-          const int rank = dq_rank(p.sched, p.causal, p.N, q, kv);
+          const int rank = dq_rank(pl.sched, p.causal, p.N, q, kv);
           if (!agree(et == 0 ? mbar_wait(bar.g5_done, it & 1, ab) : true)) {
             ok = false;
             break;

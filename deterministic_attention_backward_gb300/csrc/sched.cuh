@@ -39,10 +39,14 @@
 
 namespace dash {
 
-enum Sched : int { kAtomic = 0, kSerial = 1, kDescending = 2, kShift = 3 };
+// kShiftFill is the shift schedule on as many SMs as hold whole heads, plus DESCENDING on
+// the remaining SMs for a share of the heads (the host decides the split).
+enum Sched : int { kAtomic = 0, kSerial = 1, kDescending = 2, kShift = 3, kShiftFill = 4 };
 
-// Which visiting order a schedule uses (ATOMIC borrows the shift order when it exists).
+// Which visiting order a schedule uses (ATOMIC borrows the shift order when it exists; the
+// fill mode's shift heads use the shift order).
 DASH_HD int traversal(int sched, int causal, int N) {
+  if (sched == kShiftFill) return kShift;
   if (sched != kAtomic) return sched;
   return (!causal || (N % 2) == 0) ? kShift : kSerial;
 }

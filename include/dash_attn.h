@@ -64,12 +64,21 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           tile q adds KV blocks q, q-1, .., q+1 (mod N).  Causal mask:
  *                           Symmetric Shift -- the worker c owns KV blocks c and N-1-c,
  *                           first the dense lower-left rectangle, then the folded
- *                           triangle; requires an even N. */
+ *                           triangle; requires an even N.
+ *  DASH_SCHED_SHIFT_FILL -- the shift schedule where whole heads fill the SMs, and
+ *                           DESCENDING for a share of the heads on the SMs left over: the
+ *                           shift schedule needs all W workers of a head (W = N, or N/2
+ *                           for a causal mask) running at once, so only floor(SMs / W) * W
+ *                           SMs can hold shift heads.  The share is chosen from the SM
+ *                           count to balance the two groups.  Deterministic on a given GPU
+ *                           (the split depends on B*Hkv, N and the SM count); the schedule
+ *                           tables of dash_sched_* are those of the shift heads. */
 typedef enum {
   DASH_SCHED_ATOMIC = 0,
   DASH_SCHED_SERIAL = 1,
   DASH_SCHED_DESCENDING = 2,
-  DASH_SCHED_SHIFT = 3
+  DASH_SCHED_SHIFT = 3,
+  DASH_SCHED_SHIFT_FILL = 4
 } dash_sched_t;
 
 typedef enum {
@@ -181,6 +190,13 @@ const char *dash_status_string(dash_status_t status);
  * tile *q with KV block *kv, and its dQ partial is the rank-th addition into tile q.
  * Return -1 on unsupported arguments. */
 int dash_sched_workers(int sched, int mask, int N);
+/* How dash_attn_bwd would use a GPU with `sms` SMs for `heads` = B * H/group (batch, kv
+ * head) pairs: heads [0, *heads_a) run the requested schedule on SMs [0, *sms_a), the rest
+ * (DASH_SCHED_SHIFT_FILL only) run DESCENDING on SMs [*sms_a, *grid); *grid CTAs in all.
+ * Returns -1 where dash_attn_bwd would return DASH_ERR_UNSUPPORTED or DASH_ERR_INVALID for
+ * the schedule arguments. */
+int dash_sched_plan(int sched, int mask, int N, int heads, int sms, int *heads_a, int *sms_a,
+                    int *grid);
 int dash_sched_segments(int sched, int mask, int N, int worker);
 int dash_sched_steps(int sched, int mask, int N, int worker, int segment);
 int dash_sched_step(int sched, int mask, int N, int worker, int segment, int step, int *kv,

@@ -68,14 +68,14 @@ def test_argument_errors_are_synchronous(L):
 
 
 SCHEDS = [("serial", sc.SERIAL), ("descending", sc.DESCENDING), ("atomic", None),
-          ("shift", None)]
+          ("shift", None), ("shift_fill", None)]
 
 
 @pytest.mark.parametrize("N", [2, 4, 6, 8, 16, 64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("name,oracle_name", SCHEDS)
 def test_library_schedule_equals_oracle(L, name, oracle_name, causal, N):
-    if oracle_name is None:  # shift; the atomic reference borrows the shift traversal
+    if oracle_name is None:  # shift (and the fill mode's shift heads); atomic borrows it
         oracle_name = sc.SYMSHIFT if causal else sc.SHIFT
     table = dash.sched_table(name, causal, N)
     assert len(table) == sc.num_workers(oracle_name, causal, N)
@@ -93,6 +93,31 @@ def test_atomic_odd_causal_falls_back_to_serial_traversal(L):
     table = dash.sched_table("atomic", True, 5)
     flat = [[(kv, q) for seg in segs for kv, q, _ in seg] for segs in table]
     assert flat == [sc.visits(sc.SERIAL, True, 5, w) for w in range(5)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,heads", [(4, 64), (8, 32), (16, 16), (32, 64), (64, 32), (128, 16),
+                                     (32, 4), (128, 1)])
+def test_launch_plan(L, causal, N, heads):
+    """Plans for a 152-SM GPU: the shift group always holds whole heads (a multiple of the
+    workers per head), every head is assigned, and plain schedules use one group."""
+    sms = 152
+    W = N // 2 if causal else N
+    ha, ga, grid = dash.sched_plan("shift_fill", causal, N, heads, sms)
+    assert 1 <= ha <= heads and grid <= sms and ga <= grid
+    assert ga % W == 0 and ga >= W
+    if ha < heads:                                   # a descending group on the leftover SMs
+        assert grid == sms and ga == (sms // W) * W
+    for name in ("serial", "descending", "shift", "atomic"):
+        a, g_a, g = dash.sched_plan(name, causal, N, heads, sms)
+        assert a == heads and g_a == g
+    assert dash.sched_plan("shift", causal, N, heads, sms)[2] == min(heads * W, sms)
+
+
+def test_launch_plan_needs_a_whole_head_for_shift(L):
+    with pytest.raises(ValueError):
+        dash.sched_plan("shift", False, 160, 1, 152)
+    assert dash.sched_plan("serial", False, 160, 1, 152) == (1, 152, 152)
 
 
 def test_schedule_query_rejects_bad_arguments(L):

@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 REL_FRO = 1e-2
 MAX_ABS = 2e-2
-SCHEDULES = ["atomic", "serial", "descending", "shift"]
+SCHEDULES = ["atomic", "serial", "descending", "shift", "shift_fill"]
 
 
 @pytest.fixture(scope="module")
@@ -67,7 +67,7 @@ def test_fwd_matches_oracle(dash, shape, causal):
 @pytest.mark.parametrize("shape", SHAPES)
 def test_bwd_matches_oracle(dash, shape, causal, sched):
     N = shape[1] // 128
-    if sched == "shift" and causal and N % 2:
+    if sched.startswith("shift") and causal and N % 2:
         pytest.skip("symmetric shift needs an even number of tiles")
     c = Case(dash, *shape, causal)
     dq_r, dk_r, dv_r, _, _ = oracle.attn_bwd(*c.host, causal)
@@ -80,7 +80,7 @@ def test_bwd_matches_oracle(dash, shape, causal, sched):
 @pytest.mark.parametrize("causal", [False, True])
 def test_deterministic_schedules_bit_identical(dash, causal):
     c = Case(dash, 2, 1024, 4, 2, 128, causal, seed=1)
-    for sched in ("serial", "descending", "shift"):
+    for sched in ("serial", "descending", "shift", "shift_fill"):
         ref = [t.clone() for t in c.bwd(sched)]
         for _ in range(20):
             out = c.bwd(sched)
@@ -105,3 +105,28 @@ def test_causal_first_query_row_dq_vanishes(dash):
     for sched in SCHEDULES:
         dq, _, _ = c.bwd(sched)
         assert dq[:, 0].abs().max().item() <= 1e-2 * dq.abs().max().item(), sched
+
+
+def test_fill_mode_is_shift_plus_descending_bitwise(dash):
+    """Causal, 128 (batch, head) pairs of 32 tiles on the GPU's SMs: the fill mode runs most
+    heads with Symmetric Shift and the last ones with Descending.  Its outputs must equal,
+    bit for bit, pure SHIFT on the first group and pure DESCENDING on the second, and match
+    the oracle on one head of each group."""
+    B, S, H, D = 4, 4096, 32, 64
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    heads_a, _, _ = dash.sched_plan("shift_fill", True, S // 128, B * H, sms)
+    c = Case(dash, B, S, H, H, D, True, seed=5)
+    fill = c.bwd("shift_fill")
+    shift = c.bwd("shift")
+    desc = c.bwd("descending")
+    for hd in range(B * H):
+        b, h = divmod(hd, H)
+        want = shift if hd < heads_a else desc
+        for got, ref in zip(fill, want):
+            assert torch.equal(got[b, :, h], ref[b, :, h]), (hd, heads_a)
+    for hd in {0, B * H - 1}:
+        b, h = divmod(hd, H)
+        dq_r, dk_r, dv_r, _, _ = oracle.attn_bwd_group(*c.host, True, b=b, g=h)
+        close("dQ", fill[0][b:b + 1, :, h:h + 1], dq_r)
+        close("dK", fill[1][b:b + 1, :, h:h + 1], dk_r)
+        close("dV", fill[2][b:b + 1, :, h:h + 1], dv_r)
