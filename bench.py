@@ -53,7 +53,7 @@ WORKLOADS = {
     "gqa_causal_8b": dict(
         desc="GQA causal attention backward shaped like an 8B decoder layer: 32 query heads, "
              "8 KV heads, D=128, B=2, S=8192",
-        H=32, Hkv=8, D=128, causal=True, tokens=16384, seqs=[8192], schedule="shift",
+        H=32, Hkv=8, D=128, causal=True, tokens=16384, seqs=[8192], schedule="shift_fill",
         ref_S=2048),
     "small_b1_h2_s512_d64": dict(
         desc="full-mask attention backward, B=1, H=2, S=512, D=64 (4 KV blocks)",
@@ -119,7 +119,7 @@ class Clocks:
                 "/tmp", f"dash_clocks_{os.getpid()}.csv"), "w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None

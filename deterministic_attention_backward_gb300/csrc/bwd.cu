@@ -183,10 +183,12 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
       __syncwarp();
       last_kv = seg_it & 1;
       ++seg_it;
-      for (int g = 0; ok && g < p.G; ++g) {
-        const int h = un.hkv * p.G + g;
-        for (int t = 0; t < nsteps; ++t) {
-          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
+      // GQA: the G query heads of a step are visited back to back, so every head keeps the
+      // schedule's lock step
+      for (int t = 0; ok && t < nsteps; ++t) {
+        const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
+        for (int g = 0; g < p.G; ++g) {
+          const int h = un.hkv * p.G + g;
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
           if (!mbar_wait_warp(&bar.empty[s], ph ^ 1, ab)) {
@@ -386,8 +388,8 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
       const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
-      for (int g = 0; ok && g < p.G; ++g) {
-        for (int t = 0; t < nsteps; ++t, ++it) {
+      for (int t = 0; ok && t < nsteps; ++t) {
+        for (int g = 0; g < p.G; ++g, ++it) {
           const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
           const bool diag = p.causal && (q == kv);
           const int s = it % L::kStages;
@@ -502,9 +504,9 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
       const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
-      for (int g = 0; ok && g < p.G; ++g) {
-        const int h = un.hkv * p.G + g;
-        for (int t = 0; t < nsteps; ++t, ++it) {
+      for (int t = 0; ok && t < nsteps; ++t) {
+        for (int g = 0; g < p.G; ++g, ++it) {
+          const int h = un.hkv * p.G + g;
           const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
           int *sem = p.sem + tile_idx;
