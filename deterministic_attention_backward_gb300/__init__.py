@@ -19,7 +19,7 @@ import os
 import threading
 
 __all__ = ["fwd", "bwd", "bwd_workspace_bytes", "fwd_workspace_bytes", "status",
-           "sched_table", "sched_plan", "SCHEDULES", "lib", "DashError"]
+           "sched_table", "sched_grid", "packed_rank", "SCHEDULES", "lib", "DashError"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdash_attn.so")
@@ -30,7 +30,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CU
 EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_workspace_bytes",
            "dash_attn_bwd", "dash_attn_bwd_stages", "dash_attn_status",
            "dash_status_string", "dash_sched_workers", "dash_sched_segments", "dash_sched_steps",
-           "dash_sched_step", "dash_sched_plan", "dash_attn_bwd_noalloc"]
+           "dash_sched_step", "dash_sched_grid", "dash_sched_packed_rank",
+           "dash_attn_bwd_noalloc"]
 
 
 class DashError(RuntimeError):
@@ -82,8 +83,10 @@ def lib() -> ctypes.CDLL:
         L.dash_sched_steps.restype = i
         L.dash_sched_step.argtypes = [i, i, i, i, i, i, ip, ip, ip]
         L.dash_sched_step.restype = i
-        L.dash_sched_plan.argtypes = [i, i, i, i, i, ip, ip, ip]
-        L.dash_sched_plan.restype = i
+        L.dash_sched_grid.argtypes = [i, i, i, i, i]
+        L.dash_sched_grid.restype = i
+        L.dash_sched_packed_rank.argtypes = [i, i, i, i, i, i, i]
+        L.dash_sched_packed_rank.restype = i
         _lib = L
         return L
 
@@ -162,7 +165,7 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, schedule: str = "shift",
         check: bool = False, stages: int = ALL_STAGES):
     """Attention backward: returns (dQ, dK, dV) bf16.  ``schedule`` is one of
     ``atomic`` (non-deterministic reference), ``serial``, ``descending``, ``shift``,
-    ``shift_fill`` (shift on whole heads, descending on the SMs left over).
+    ``shift_fill`` (packed shift: all SMs busy, heads split across rounds run in phases).
     ``stages`` (PROLOGUE | TILES | EPILOGUE) launches only part of the work, in order, on
     the same workspace (for timing the tile kernel on its own)."""
     import torch
@@ -196,15 +199,20 @@ def status(workspace, stream=None):
     _check(lib().dash_attn_status(workspace.data_ptr(), _stream_ptr(stream)), "device status")
 
 
-def sched_plan(schedule: str, causal: bool, N: int, heads: int, sms: int):
-    """(heads on the requested schedule, SMs they use, total CTAs) for ``heads`` (batch,
-    kv-head) pairs on a GPU with ``sms`` SMs; the rest run DESCENDING (fill mode only)."""
-    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    code = lib().dash_sched_plan(SCHEDULES[schedule], int(bool(causal)), N, heads, sms,
-                                 ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
-    if code != 0:
+def sched_grid(schedule: str, causal: bool, N: int, heads: int, sms: int) -> int:
+    """CTAs of the tile kernel for ``heads`` (batch, kv-head) pairs on ``sms`` SMs."""
+    g = lib().dash_sched_grid(SCHEDULES[schedule], int(bool(causal)), N, heads, sms)
+    if g < 0:
         raise ValueError("unsupported schedule arguments")
-    return a.value, b.value, c.value
+    return g
+
+
+def packed_rank(causal: bool, N: int, heads: int, grid: int, head: int, q: int, kv: int) -> int:
+    """Position of KV block kv's partial in dQ tile q of ``head`` under the packed shift."""
+    r = lib().dash_sched_packed_rank(int(bool(causal)), N, heads, grid, head, q, kv)
+    if r < 0:
+        raise ValueError("bad arguments")
+    return r
 
 
 def sched_table(schedule: str, causal: bool, N: int):

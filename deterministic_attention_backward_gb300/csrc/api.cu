@@ -117,55 +117,21 @@ BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
 unsigned long long *g_trace = nullptr;  // development trace build only
 #endif
 
-// How the backward tile kernel's grid is used: heads [0, heads_a) run schedule sched_a on
-// CTAs [0, grid_a), the remaining heads run sched_b on CTAs [grid_a, grid).
+// How the backward tile kernel's grid is used: the workers of all heads, head-major, dealt
+// round-robin to `grid` CTAs.
 struct LaunchPlan {
-  int sched_a, workers_a, heads_a, grid_a, sched_b, workers_b, grid;
+  int sched, workers, grid, packed;
 };
 
 // False when a shift schedule cannot have every worker of a head resident at once.
 bool make_plan(int sched, int causal, int N, int heads, int sms, LaunchPlan *pl) {
-  const int trav = dash::traversal(sched, causal, N);
-  const int W = dash::sched_workers(trav, causal, N);
-  const long long total = (long long)heads * W;
-  pl->sched_a = pl->sched_b = trav;
-  pl->workers_a = pl->workers_b = W;
-  pl->heads_a = heads;
-  pl->grid = pl->grid_a = (int)(total < sms ? total : sms);
+  pl->sched = dash::traversal(sched, causal, N);
+  pl->workers = dash::sched_workers(pl->sched, causal, N);
+  const long long total = (long long)heads * pl->workers;
+  pl->grid = (int)(total < sms ? total : sms);
+  pl->packed = sched == DASH_SCHED_SHIFT_FILL;
   const bool shift = sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL;
-  if (shift && W > sms) return false;
-  if (sched != DASH_SCHED_SHIFT_FILL) return true;
-  const int k = sms / W;  // whole heads per round of the shift group
-  if (heads <= k) return true;
-  const int grid_a = k * W, L = sms - grid_a;
-  if (L == 0) return true;
-  // Group B runs DESCENDING (no co-residency needed) on the L leftover SMs.  Its head count
-  // balances the estimated finish times; tile steps per SM of DESCENDING are taken as 0.7
-  // of the shift schedule's (it pays the serialized pipeline fill of each head).
-  const double unit_a = causal ? N + 1.0 : (double)N;              // steps of a shift worker
-  const double head_work = causal ? N * (N + 1) / 2.0 : (double)N * N;  // tile steps per head
-  const double eff_b = 0.7;
-  int best_hb = 0;
-  double best = std::ceil((double)heads / k) * unit_a;
-  for (int hb = 1; hb < heads; ++hb) {
-    const double ta = std::ceil((double)(heads - hb) / k) * unit_a;
-    const double tb = hb * head_work / (L * eff_b);
-    const double t = ta > tb ? ta : tb;
-    if (t < best) {
-      best = t;
-      best_hb = hb;
-    }
-  }
-  pl->grid_a = grid_a;
-  if (best_hb == 0) {  // whole-head rounds only, the leftover SMs stay idle
-    pl->grid = grid_a;
-    return true;
-  }
-  pl->heads_a = heads - best_hb;
-  pl->grid = sms;
-  pl->sched_b = dash::kDescending;
-  pl->workers_b = N;
-  return true;
+  return !(shift && pl->workers > sms);
 }
 
 float resolve_scale(float scale, int D) {
@@ -285,12 +251,9 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   p.N = N;
   p.causal = causal;
   p.heads = B * Hkv;
-  p.sched_a = plan.sched_a;
-  p.workers_a = plan.workers_a;
-  p.heads_a = plan.heads_a;
-  p.grid_a = plan.grid_a;
-  p.sched_b = plan.sched_b;
-  p.workers_b = plan.workers_b;
+  p.sched = plan.sched;
+  p.workers = plan.workers;
+  p.packed = plan.packed;
   p.scale_log2 = sc * dash::kLog2e;
   p.scale = sc;
 #ifdef DASH_TRACE_BUILD
@@ -362,16 +325,21 @@ static bool sched_args_ok(int sched, int mask, int N) {
   return true;
 }
 
-int dash_sched_plan(int sched, int mask, int N, int heads, int sms, int *heads_a, int *sms_a,
-                    int *grid) {
+int dash_sched_grid(int sched, int mask, int N, int heads, int sms) {
   LaunchPlan pl;
   if (!sched_args_ok(sched, mask, N) || heads <= 0 || sms <= 0 ||
       !make_plan(sched, mask, N, heads, sms, &pl))
     return -1;
-  if (heads_a) *heads_a = pl.heads_a;
-  if (sms_a) *sms_a = pl.grid_a;
-  if (grid) *grid = pl.grid;
-  return 0;
+  return pl.grid;
+}
+
+int dash_sched_packed_rank(int mask, int N, int heads, int grid, int head, int q, int kv) {
+  if (!sched_args_ok(DASH_SCHED_SHIFT_FILL, mask, N) || heads <= 0 || head < 0 ||
+      head >= heads || q < 0 || q >= N || kv < 0 || kv >= N || (mask && kv > q))
+    return -1;
+  const int W = dash::sched_workers(dash::kShift, mask, N);
+  if (grid < W || grid > heads * W) return -1;
+  return dash::packed_rank(mask, N, grid, head, q, kv);
 }
 
 int dash_sched_workers(int sched, int mask, int N) {

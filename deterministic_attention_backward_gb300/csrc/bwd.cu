@@ -90,22 +90,18 @@ struct RegSplit {
   static_assert(kCtl + 2 * kSoftmax + kEpi == 4 * kLaunch, "register split must sum to the launch");
 };
 
-// Work of this CTA.  The heads are split into two groups with their own schedule and their
-// own CTAs (the split is a single group unless the fill mode is used): group A are heads
-// [0, heads_a) on CTAs [0, grid_a), group B the remaining heads on the remaining CTAs.
-// Within a group, worker u of the group runs on CTA (u mod group size), in order.
+// Work of this CTA: worker u (head-major over all heads) runs on CTA (u mod grid), in order.
 struct Plan {
   int sched, W, first, stride, nunits, head_off;
 };
 __device__ __forceinline__ Plan cta_plan(const BwdParams &p) {
   Plan pl;
-  const bool grp_b = (int)blockIdx.x >= p.grid_a;
-  pl.sched = grp_b ? p.sched_b : p.sched_a;
-  pl.W = grp_b ? p.workers_b : p.workers_a;
-  pl.first = grp_b ? (int)blockIdx.x - p.grid_a : (int)blockIdx.x;
-  pl.stride = grp_b ? (int)gridDim.x - p.grid_a : p.grid_a;
-  pl.nunits = (grp_b ? p.heads - p.heads_a : p.heads_a) * pl.W;
-  pl.head_off = grp_b ? p.heads_a : 0;
+  pl.sched = p.sched;
+  pl.W = p.workers;
+  pl.first = (int)blockIdx.x;
+  pl.stride = (int)gridDim.x;
+  pl.nunits = p.heads * pl.W;
+  pl.head_off = 0;
   return pl;
 }
 
@@ -500,6 +496,11 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
+    // packed shift: the phase of this worker within its head (fixed for the unit)
+    int ph_lo = 0, ph_hi = pl.W;
+    if (p.packed)
+      packed_phase(pl.W, (int)gridDim.x, un.b * p.Hkv + un.hkv, un.w, &ph_lo, &ph_hi);
+    const bool split = p.packed && (ph_hi - ph_lo) != pl.W;
     const int nseg = sched_segments(pl.sched, p.causal);
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
@@ -510,7 +511,18 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
           int *sem = p.sem + tile_idx;
-          const int rank = dq_rank(pl.sched, p.causal, p.N, q, kv);
+          int rank;
+          if (!split) {  // the head's workers share one round: plain shift order
+            rank = dq_rank(pl.sched, p.causal, p.N, q, kv);
+          } else if (!p.causal) {
+            rank = packed_rank(0, p.N, (int)gridDim.x, un.b * p.Hkv + un.hkv, q, kv);
+          } else {  // count the phase's earlier contributions, a slice per lane
+            const int per = (ph_hi - ph_lo + 31) >> 5;
+            const int cb = ph_lo + lane * per;
+            const int ce = cb + per < ph_hi ? cb + per : ph_hi;
+            const int n = cb < ce ? packed_count_in_phase(1, p.N, q, kv, cb, ce) : 0;
+            rank = packed_count_before(1, p.N, q, ph_lo) + (int)__reduce_add_sync(0xffffffffu, n);
+          }
           if (!agree(et == 0 ? mbar_wait(bar.g5_done, it & 1, ab) : true)) {
             ok = false;
             break;

@@ -33,10 +33,10 @@ struct BwdParams {
   __nv_bfloat16 *dv;  // [B,S,Hkv,D]
   int B, S, H, Hkv, G, N;
   int causal;
-  int heads;                 // B * Hkv (b, kv head) pairs
-  int sched_a, workers_a;    // group A: schedule, workers per head
-  int heads_a, grid_a;       //   heads [0, heads_a) on CTAs [0, grid_a)
-  int sched_b, workers_b;    // group B: the remaining heads on the remaining CTAs
+  int heads;    // B * Hkv (b, kv head) pairs
+  int sched;    // visiting order of the workers (sched.cuh)
+  int workers;  // workers per head
+  int packed;   // dQ ranks of the packed shift (workers dealt round-robin over the grid)
   float scale_log2; // scale * log2(e)
   float scale;
   unsigned long long *trace;  // development trace build only: [64 steps][32 events] clock64

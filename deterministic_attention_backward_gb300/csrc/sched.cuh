@@ -102,4 +102,82 @@ DASH_HD int dq_rank(int sched, int causal, int N, int q, int kv) {
   return kv;
 }
 
+// ---------------------------------------------------------------------------------------
+// Packed shift (kShiftFill).  The shift workers of all heads are laid out head-major and
+// dealt round-robin to the P CTAs of the grid; every CTA runs its workers one per round.
+// A head whose workers fall into two rounds runs as two lock-step phases (the workers of
+// the earlier round first).  The visiting order of a worker is its head's shift order; the
+// accumulation order of a dQ tile is the time order of its contributions: earlier phase
+// first, then the step within the phase.  With W | P (no head split) this is exactly the
+// shift order above.
+
+// Worker (within its head) that owns KV block kv under the shift schedule.
+DASH_HD int shift_worker_of(int causal, int N, int kv) {
+  return (causal && kv >= (N >> 1)) ? N - 1 - kv : kv;
+}
+// Step, within its worker's program, at which the shift worker owning block kv visits
+// query tile q; -1 if the tile is masked for that block.
+DASH_HD int shift_visit_step(int causal, int N, int kv, int q) {
+  if (!causal) {
+    const int t = q - kv;
+    return t < 0 ? t + N : t;
+  }
+  if (q < kv) return -1;
+  const int h = N >> 1;
+  if (kv < h) {  // worker c = kv, first segment
+    if (q >= h) {
+      const int t = q - h - kv;
+      return t < 0 ? t + h : t;
+    }
+    return h + (q - kv);
+  }
+  const int c = N - 1 - kv;  // worker c, second segment (block N-1-c)
+  return (N - c) + (N - 1 - q);
+}
+// The phase [lo, hi) of worker w of head hd: the workers of hd in w's round.
+DASH_HD void packed_phase(int W, int P, int hd, int w, int *lo, int *hi) {
+  const long long s0 = (long long)hd * W;
+  const long long round = (s0 + w) / P;
+  long long a = round * P - s0, b = (round + 1) * P - s0;
+  *lo = (int)(a < 0 ? 0 : a);
+  *hi = (int)(b > W ? W : b);
+}
+// Contributions to tile q that precede (q, kv) and come from the phase's other workers
+// [c_begin, c_end) (a slice of the phase, so that the count can be split across threads).
+DASH_HD int packed_count_in_phase(int causal, int N, int q, int kv, int c_begin, int c_end) {
+  const int tme = shift_visit_step(causal, N, kv, q);
+  int n = 0;
+  for (int c = c_begin; c < c_end; ++c) {
+    const int t1 = shift_visit_step(causal, N, c, q);
+    if (t1 >= 0 && t1 < tme) ++n;
+    if (causal) {
+      const int t2 = shift_visit_step(causal, N, N - 1 - c, q);
+      if (t2 >= 0 && t2 < tme) ++n;
+    }
+  }
+  return n;
+}
+// Contributions to tile q from the workers [0, lo) of earlier rounds (all allowed blocks).
+DASH_HD int packed_count_before(int causal, int N, int q, int lo) {
+  if (!causal) return lo;
+  const int a = lo < q + 1 ? lo : q + 1;             // blocks c <= q, c < lo
+  const int b = lo - (N - 1 - q);                    // blocks N-1-c <= q, c < lo
+  return a + (b > 0 ? b : 0);
+}
+// Rank of block kv in dQ tile q of head hd (full mask in closed form; the causal count is
+// the same definition evaluated over the phase's workers).
+DASH_HD int packed_rank(int causal, int N, int P, int hd, int q, int kv) {
+  const int W = causal ? (N >> 1) : N;
+  int lo, hi;
+  packed_phase(W, P, hd, shift_worker_of(causal, N, kv), &lo, &hi);
+  if (!causal) {
+    const int Wp = hi - lo, k = kv - lo;
+    int base = (q - lo) % N;
+    base = base < 0 ? base + N : base;
+    const int in_phase = (base >= Wp - 1) ? Wp - 1 - k : (k <= base ? base - k : base + Wp - k);
+    return lo + in_phase;
+  }
+  return packed_count_before(causal, N, q, lo) + packed_count_in_phase(causal, N, q, kv, lo, hi);
+}
+
 }  // namespace dash

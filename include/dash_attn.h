@@ -65,14 +65,17 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           Symmetric Shift -- the worker c owns KV blocks c and N-1-c,
  *                           first the dense lower-left rectangle, then the folded
  *                           triangle; requires an even N.
- *  DASH_SCHED_SHIFT_FILL -- the shift schedule where whole heads fill the SMs, and
- *                           DESCENDING for a share of the heads on the SMs left over: the
- *                           shift schedule needs all W workers of a head (W = N, or N/2
- *                           for a causal mask) running at once, so only floor(SMs / W) * W
- *                           SMs can hold shift heads.  The share is chosen from the SM
- *                           count to balance the two groups.  Deterministic on a given GPU
- *                           (the split depends on B*Hkv, N and the SM count); the schedule
- *                           tables of dash_sched_* are those of the shift heads. */
+ *  DASH_SCHED_SHIFT_FILL -- packed Shift Scheduling: the shift workers of all heads (W per
+ *                           head: N, or N/2 for the causal mask) are dealt round-robin,
+ *                           head-major, to every SM.  When W does not divide the SM count
+ *                           a head's workers can fall into two consecutive rounds; such a
+ *                           head runs as two lock-step phases, and each of its dQ tiles adds
+ *                           the earlier phase's partials first, then the later phase's, each
+ *                           phase in its shift (step) order.  Heads inside one round get
+ *                           exactly the DASH_SCHED_SHIFT order.  Keeps every SM busy where
+ *                           plain SHIFT leaves SMs waiting for a head's remaining workers.
+ *                           Deterministic for a given SM count (dash_sched_grid,
+ *                           dash_sched_packed_rank give the order). */
 typedef enum {
   DASH_SCHED_ATOMIC = 0,
   DASH_SCHED_SERIAL = 1,
@@ -190,13 +193,14 @@ const char *dash_status_string(dash_status_t status);
  * tile *q with KV block *kv, and its dQ partial is the rank-th addition into tile q.
  * Return -1 on unsupported arguments. */
 int dash_sched_workers(int sched, int mask, int N);
-/* How dash_attn_bwd would use a GPU with `sms` SMs for `heads` = B * H/group (batch, kv
- * head) pairs: heads [0, *heads_a) run the requested schedule on SMs [0, *sms_a), the rest
- * (DASH_SCHED_SHIFT_FILL only) run DESCENDING on SMs [*sms_a, *grid); *grid CTAs in all.
- * Returns -1 where dash_attn_bwd would return DASH_ERR_UNSUPPORTED or DASH_ERR_INVALID for
- * the schedule arguments. */
-int dash_sched_plan(int sched, int mask, int N, int heads, int sms, int *heads_a, int *sms_a,
-                    int *grid);
+/* Number of CTAs dash_attn_bwd launches for its tile kernel on a GPU with `sms` SMs, for
+ * `heads` = B * H/group (batch, kv head) pairs; -1 where dash_attn_bwd would reject the
+ * schedule arguments (e.g. a shift schedule whose workers per head exceed the SMs). */
+int dash_sched_grid(int sched, int mask, int N, int heads, int sms);
+/* DASH_SCHED_SHIFT_FILL: position of KV block kv's partial in dQ tile q of head `head`
+ * (0 <= head < heads) when the tile kernel runs on `grid` CTAs (dash_sched_grid); -1 on
+ * bad arguments or a masked (q, kv). */
+int dash_sched_packed_rank(int mask, int N, int heads, int grid, int head, int q, int kv);
 int dash_sched_segments(int sched, int mask, int N, int worker);
 int dash_sched_steps(int sched, int mask, int N, int worker, int segment);
 int dash_sched_step(int sched, int mask, int N, int worker, int segment, int step, int *kv,

@@ -138,3 +138,35 @@ def critical_path(sched: str, causal: bool, N: int) -> int:
             raise RuntimeError("schedule deadlocks in the unit-step model")
         pending = rest
     return max(finish.values())
+
+
+# ---------------------------------------------------------------------------------------
+# Packed shift: the shift workers of all heads are laid out one after another (head-major)
+# and dealt round-robin to P processors; processor p runs its workers in order, one per
+# round, every round taking the same time (lock step).  A head whose workers fall into two
+# rounds runs as two phases.  The accumulation order of every dQ tile is the time order of
+# its contributions (round, then step); the visiting order of each worker is the shift
+# order of its head.  This is the shift schedule of the pages for a processor count that
+# is not a multiple of the workers per head.
+def packed_rounds(sched: str, causal: bool, N: int, heads: int, P: int):
+    """(head, worker) -> round index."""
+    W = num_workers(sched, causal, N)
+    return {(hd, w): (hd * W + w) // P for hd in range(heads) for w in range(W)}
+
+
+def packed_reduction_order(sched: str, causal: bool, N: int, heads: int, P: int):
+    """(head, q) -> KV blocks in the order their partials are added."""
+    W = num_workers(sched, causal, N)
+    rounds = packed_rounds(sched, causal, N, heads, P)
+    steps_per_round = max(len(visits(sched, causal, N, w)) for w in range(W))
+    arrivals: dict = {}
+    for (hd, w), r in rounds.items():
+        for t, (kv, q) in enumerate(visits(sched, causal, N, w)):
+            arrivals.setdefault((hd, q), []).append((r * steps_per_round + t, kv))
+    out = {}
+    for key, a in arrivals.items():
+        a.sort()
+        times = [t for t, _ in a]
+        assert len(set(times)) == len(times), "two contributions to one tile at one time"
+        out[key] = [kv for _, kv in a]
+    return out

@@ -96,28 +96,31 @@ def test_atomic_odd_causal_falls_back_to_serial_traversal(L):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N,heads", [(4, 64), (8, 32), (16, 16), (32, 64), (64, 32), (128, 16),
-                                     (32, 4), (128, 1)])
-def test_launch_plan(L, causal, N, heads):
-    """Plans for a 152-SM GPU: the shift group always holds whole heads (a multiple of the
-    workers per head), every head is assigned, and plain schedules use one group."""
-    sms = 152
+@pytest.mark.parametrize("N,heads,P", [(8, 5, 12), (8, 3, 8), (16, 4, 24), (4, 9, 10), (32, 3, 38),
+                                       (32, 64, 152), (64, 8, 152), (16, 20, 152)])
+def test_packed_ranks_equal_oracle(L, causal, N, heads, P):
+    """The library's packed-shift ranks equal the oracle's lock-step simulation of the
+    workers dealt round-robin to P CTAs."""
     W = N // 2 if causal else N
-    ha, ga, grid = dash.sched_plan("shift_fill", causal, N, heads, sms)
-    assert 1 <= ha <= heads and grid <= sms and ga <= grid
-    assert ga % W == 0 and ga >= W
-    if ha < heads:                                   # a descending group on the leftover SMs
-        assert grid == sms and ga == (sms // W) * W
-    for name in ("serial", "descending", "shift", "atomic"):
-        a, g_a, g = dash.sched_plan(name, causal, N, heads, sms)
-        assert a == heads and g_a == g
-    assert dash.sched_plan("shift", causal, N, heads, sms)[2] == min(heads * W, sms)
+    if P > heads * W:
+        P = heads * W
+    order = sc.packed_reduction_order(sc.SYMSHIFT if causal else sc.SHIFT, causal, N, heads, P)
+    for (hd, q), kvs in order.items():
+        for r, kv in enumerate(kvs):
+            assert dash.packed_rank(causal, N, heads, P, hd, q, kv) == r
 
 
-def test_launch_plan_needs_a_whole_head_for_shift(L):
+@pytest.mark.parametrize("causal", [False, True])
+def test_grid_sizes(L, causal):
+    N, heads, sms = 32, 64, 152
+    W = N // 2 if causal else N
+    for name in ("serial", "descending", "shift", "shift_fill", "atomic"):
+        w = W if name in ("shift", "shift_fill", "atomic") else N
+        assert dash.sched_grid(name, causal, N, heads, sms) == min(heads * w, sms)
+    assert dash.sched_grid("shift_fill", causal, N, 1, sms) == W
     with pytest.raises(ValueError):
-        dash.sched_plan("shift", False, 160, 1, 152)
-    assert dash.sched_plan("serial", False, 160, 1, 152) == (1, 152, 152)
+        dash.sched_grid("shift", False, 160, 1, 152)
+    assert dash.sched_grid("serial", False, 160, 1, 152) == 152
 
 
 def test_schedule_query_rejects_bad_arguments(L):

@@ -107,26 +107,27 @@ def test_causal_first_query_row_dq_vanishes(dash):
         assert dq[:, 0].abs().max().item() <= 1e-2 * dq.abs().max().item(), sched
 
 
-def test_fill_mode_is_shift_plus_descending_bitwise(dash):
-    """Causal, 128 (batch, head) pairs of 32 tiles on the GPU's SMs: the fill mode runs most
-    heads with Symmetric Shift and the last ones with Descending.  Its outputs must equal,
-    bit for bit, pure SHIFT on the first group and pure DESCENDING on the second, and match
-    the oracle on one head of each group."""
+def test_packed_shift_bitwise_where_heads_fit_and_oracle_where_split(dash):
+    """Causal, 128 (batch, head) pairs of 16 shift workers dealt to the GPU's SMs: heads
+    whose workers share one round get exactly the SHIFT order (bit-identical outputs); a head
+    split across two rounds runs in two phases and still matches the oracle."""
     B, S, H, D = 4, 4096, 32, 64
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    heads_a, _, _ = dash.sched_plan("shift_fill", True, S // 128, B * H, sms)
+    N, heads = S // 128, B * H
+    W = N // 2
+    grid = dash.sched_grid("shift_fill", True, N, heads, sms)
+    split = [hd for hd in range(heads) if (hd * W) // grid != (hd * W + W - 1) // grid]
+    whole = [hd for hd in range(heads) if hd not in split]
     c = Case(dash, B, S, H, H, D, True, seed=5)
-    fill = c.bwd("shift_fill")
+    packed = c.bwd("shift_fill")
     shift = c.bwd("shift")
-    desc = c.bwd("descending")
-    for hd in range(B * H):
+    for hd in whole:
         b, h = divmod(hd, H)
-        want = shift if hd < heads_a else desc
-        for got, ref in zip(fill, want):
-            assert torch.equal(got[b, :, h], ref[b, :, h]), (hd, heads_a)
-    for hd in {0, B * H - 1}:
+        for got, ref in zip(packed, shift):
+            assert torch.equal(got[b, :, h], ref[b, :, h]), hd
+    for hd in ([split[0]] if split else []) + [whole[0]]:
         b, h = divmod(hd, H)
         dq_r, dk_r, dv_r, _, _ = oracle.attn_bwd_group(*c.host, True, b=b, g=h)
-        close("dQ", fill[0][b:b + 1, :, h:h + 1], dq_r)
-        close("dK", fill[1][b:b + 1, :, h:h + 1], dk_r)
-        close("dV", fill[2][b:b + 1, :, h:h + 1], dv_r)
+        close("dQ", packed[0][b:b + 1, :, h:h + 1], dq_r)
+        close("dK", packed[1][b:b + 1, :, h:h + 1], dk_r)
+        close("dV", packed[2][b:b + 1, :, h:h + 1], dv_r)

@@ -93,3 +93,18 @@ def test_symshift_rejects_odd_or_full():
         sc.visits(sc.SYMSHIFT, True, 5, 0)
     with pytest.raises(ValueError):
         sc.visits(sc.SYMSHIFT, False, 4, 0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,heads,P", [(8, 5, 12), (8, 3, 8), (16, 4, 24), (4, 9, 10), (32, 3, 38)])
+def test_packed_shift_is_conflict_free_and_reduces_to_shift(causal, N, heads, P):
+    sched = sc.SYMSHIFT if causal else sc.SHIFT
+    order = sc.packed_reduction_order(sched, causal, N, heads, P)
+    W = sc.num_workers(sched, causal, N)
+    rounds = sc.packed_rounds(sched, causal, N, heads, P)
+    for hd in range(heads):
+        for q in range(N):
+            assert sorted(order[(hd, q)]) == [kv for kv in range(N) if sc.allowed(causal, q, kv)]
+        if len({rounds[(hd, w)] for w in range(W)}) == 1:     # a head inside one round
+            plain = sc.reduction_order(sched, causal, N)
+            assert all(order[(hd, q)] == plain[q] for q in range(N))
