@@ -398,7 +398,8 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
           tc_fence_after();
           const float *lse_s = reinterpret_cast<const float *>(smem + L::offLSE + s * kTile * 4);
           const float *dvec_s = reinterpret_cast<const float *>(smem + L::offDVEC + s * kTile * 4);
-          float pf[64];
+          // P^T of this half, packed bf16x2 (the values G3 consumes); dS uses the same bf16 P
+          uint32_t pk[32];
           {
             uint32_t sv[64];
             tmem_ld32(tmem + lane_off + L::tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
@@ -412,15 +413,22 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
             for (int c = 0; c < 64; c += 4) {
               const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + c0 + c);
               const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              float pv[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                float pv = ex2_approx(fmaf(__uint_as_float(sv[c + e]), p.scale_log2, -lv[e]));
-                if (diag && (c0 + c + e) < r) pv = 0.f;
-                pf[c + e] = pv;
+                pv[e] = ex2_approx(fmaf(__uint_as_float(sv[c + e]), p.scale_log2, -lv[e]));
+                if (diag && (c0 + c + e) < r) pv[e] = 0.f;
               }
+              pk[c / 2] = pack_bf16(pv[0], pv[1]);
+              pk[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
             }
           }
           if (lane == 0 && warp == 4 + 4 * x) DASH_TRACE(p, 7 + 4 * x);
+          // Dvec of the first chunk into registers while dP^T is still being computed
+          float dv[32];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4 *>(&dv[c]) = *reinterpret_cast<const float4 *>(dvec_s + c0 + c);
           if (!mbar_wait_warp(bar.dp_full, par, ab)) {
             ok = false;
             break;
@@ -430,24 +438,24 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             const uint32_t col = L::tDP + c0 + 32 * ch;
-            uint32_t dpv[32], pk[16], dk[16];
+            uint32_t dpv[32], dk[16];
             tmem_ld32(tmem + lane_off + col, dpv);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              const float4 d4 = *reinterpret_cast<const float4 *>(dvec_s + c0 + 32 * ch + c);
-              const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-              float ds[4];
+            for (int m = 0; m < 16; ++m) {
+              const uint32_t w = pk[16 * ch + m];
+              const float p0 = __uint_as_float(w << 16), p1 = __uint_as_float(w & 0xFFFF0000u);
+              dk[m] = pack_bf16(p0 * (__uint_as_float(dpv[2 * m]) - dv[2 * m]),
+                                p1 * (__uint_as_float(dpv[2 * m + 1]) - dv[2 * m + 1]));
+            }
+            if (ch == 0) {  // next chunk's Dvec
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                ds[e] = pf[32 * ch + c + e] * (__uint_as_float(dpv[c + e]) - dvv[e]);
-              dk[c / 2] = pack_bf16(ds[0], ds[1]);
-              dk[c / 2 + 1] = pack_bf16(ds[2], ds[3]);
-              pk[c / 2] = pack_bf16(pf[32 * ch + c], pf[32 * ch + c + 1]);
-              pk[c / 2 + 1] = pack_bf16(pf[32 * ch + c + 2], pf[32 * ch + c + 3]);
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4 *>(&dv[c]) =
+                    *reinterpret_cast<const float4 *>(dvec_s + c0 + 32 + c);
             }
             // both into the chunk's own (already read) dP^T columns: P^T, then dS^T
-            tmem_st16(tmem + lane_off + col, pk);
+            tmem_st16(tmem + lane_off + col, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * ch]));
             tmem_st16(tmem + lane_off + col + 16, dk);
             // dS into shared memory as the MN-major A operand of G5: row r of box x,
             // 16-byte chunk (4ch + j) at position (4ch + j) ^ (r % 8)
