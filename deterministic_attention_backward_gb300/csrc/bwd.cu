@@ -30,9 +30,11 @@
 // The softmax-gradient warpgroups read S^T(t) and release its columns at once, so G1(t+1)
 // runs while they compute P and dS; they write P^T and dS^T over the dP^T columns they have
 // just read.  The epilogue copies the dQ partial to registers first and waits for its
-// turn on the semaphore afterwards, so a waiting reduction does not hold tensor memory;
-// each epilogue thread then adds 1 to the semaphore with release semantics after its own
-// reductions, and the next contributor goes when the count reaches 128 x its rank.
+// turn on the semaphore afterwards, so a waiting reduction does not hold tensor memory.
+// The semaphore of a dQ tile counts the partials added to it; a poller warp watches the
+// semaphores of this CTA's coming steps ahead of time, so the epilogue usually finds its
+// turn already taken when the drain ends.  After the warpgroup's reductions one thread
+// adds 1 with release semantics.
 //
 // Warp roles (512 threads; register budgets set per warpgroup with setmaxnreg):
 //   warp 0      TMA producer (converged warp, one elected lane issues): K_j, V_j per
@@ -40,6 +42,7 @@
 //   warp 1      MMA issuer (converged warp, one elected lane issues): G1..G5 and the
 //               tcgen05.commit arrivals
 //   warp 2      allocates / frees the 512 TMEM columns
+//   warp 3      deterministic modes: semaphore poller (acquires the epilogue's turns ahead)
 //   warps 4-11  two softmax-gradient warpgroups; warpgroup w handles query columns
 //               [64w, 64w+64) of the tile, thread = KV row (TMEM lane)
 //   warps 12-15 epilogue warpgroup: dQ partial TMEM -> ordered/atomic fp32 reduction in
@@ -441,6 +444,7 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
             uint32_t dpv[32], dk[16];
             tmem_ld32(tmem + lane_off + col, dpv);
             tmem_ld_wait();
+            if (lane == 0 && warp == 4) DASH_TRACE(p, 18 + 4 * ch);
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
               const uint32_t w = pk[16 * ch + m];
@@ -454,9 +458,11 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
                 *reinterpret_cast<float4 *>(&dv[c]) =
                     *reinterpret_cast<const float4 *>(dvec_s + c0 + 32 + c);
             }
+            if (lane == 0 && warp == 4) DASH_TRACE(p, 19 + 4 * ch);
             // both into the chunk's own (already read) dP^T columns: P^T, then dS^T
             tmem_st16(tmem + lane_off + col, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * ch]));
             tmem_st16(tmem + lane_off + col + 16, dk);
+            if (lane == 0 && warp == 4) DASH_TRACE(p, 20 + 4 * ch);
             // dS into shared memory as the MN-major A operand of G5: row r of box x,
             // 16-byte chunk (4ch + j) at position (4ch + j) ^ (r % 8)
 #pragma unroll
@@ -465,9 +471,12 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
               *reinterpret_cast<uint4 *>(ds_row + ((cj ^ (r & 7)) << 4)) =
                   make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
             }
+            if (lane == 0 && warp == 4) DASH_TRACE(p, 21 + 4 * ch);
           }
           fence_proxy_async_smem();
+          if (lane == 0 && warp == 4) DASH_TRACE(p, 26);
           tmem_st_wait();
+          if (lane == 0 && warp == 4) DASH_TRACE(p, 27);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -482,6 +491,72 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
 }
 
 // ---------------------------------------------------------------------------------------
+// The dQ-tile order of one worker: the rank of its contribution to query tile q from KV
+// block kv.  Plain shift order when the head's workers share one round of the grid, else
+// the packed-shift count (full mask in closed form; causal: the phase's earlier
+// contributions, counted a slice per lane, so all 32 lanes of the warp must call it).
+struct UnitOrder {
+  int ph_lo, ph_hi, hd;
+  bool split;
+};
+__device__ __forceinline__ UnitOrder unit_order(const BwdParams &p, const Plan &pl, const Unit &un) {
+  UnitOrder o;
+  o.ph_lo = 0;
+  o.ph_hi = pl.W;
+  o.hd = un.b * p.Hkv + un.hkv;
+  if (p.packed) packed_phase(pl.W, (int)gridDim.x, o.hd, un.w, &o.ph_lo, &o.ph_hi);
+  o.split = p.packed && (o.ph_hi - o.ph_lo) != pl.W;
+  return o;
+}
+__device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, const UnitOrder &o,
+                                         int q, int kv, int lane) {
+  if (!o.split) return dq_rank(pl.sched, p.causal, p.N, q, kv);
+  if (!p.causal) return packed_rank(0, p.N, (int)gridDim.x, o.hd, q, kv);
+  const int per = (o.ph_hi - o.ph_lo + 31) >> 5;
+  const int cb = o.ph_lo + lane * per;
+  const int ce = cb + per < o.ph_hi ? cb + per : o.ph_hi;
+  const int n = cb < ce ? packed_count_in_phase(1, p.N, q, kv, cb, ce) : 0;
+  return packed_count_before(1, p.N, q, o.ph_lo) + (int)__reduce_add_sync(0xffffffffu, n);
+}
+
+// Semaphore poller (warp 3, deterministic modes): walks this CTA's steps in the
+// epilogue's order and, for each, waits until the step's dQ tile semaphore equals the
+// step's rank, then publishes the number of steps acquired so far in shared memory.  The
+// L2 round trips of the polling thus overlap the computation of the dQ partial instead
+// of following its drain.  It runs ahead of the epilogue by any number of steps; that is
+// safe because a tile's count only grows.
+template <int D>
+__device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &ab) {
+  using L = BwdLayout<D>;
+  const int lane = lane_id();
+  uint32_t *seen = reinterpret_cast<uint32_t *>(smem + L::offMisc + 16);
+  uint32_t it = 0;
+  const Plan pl = cta_plan(p);
+  for (int u = pl.first; u < pl.nunits; u += pl.stride) {
+    const Unit un = decode_unit(p, pl, u);
+    const UnitOrder o = unit_order(p, pl, un);
+    const int nseg = sched_segments(pl.sched, p.causal);
+    for (int seg = 0; seg < nseg; ++seg) {
+      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
+      for (int t = 0; t < nsteps; ++t) {
+        const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
+        const int rank = step_rank(p, pl, o, q, kv, lane);
+        for (int g = 0; g < p.G; ++g, ++it) {
+          const int h = un.hkv * p.G + g;
+          const int *sem = p.sem + (size_t)(un.b * p.H + h) * p.N + q;
+          int ok = 1;
+          if (lane == 0) {
+            ok = sem_wait(sem, rank, ab) ? 1 : 0;
+            if (ok) st_release_cta_shared(seen, it + 1);
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        }
+      }
+    }
+  }
+}
+
 template <int D, bool DET>
 __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D> &bar,
                              const Abort &ab) {
@@ -501,14 +576,10 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
     named_bar_sync(1, 128);
     return decision[dec++ & 1] != 0;
   };
+  const uint32_t *seen = reinterpret_cast<const uint32_t *>(smem + L::offMisc + 16);
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    // packed shift: the phase of this worker within its head (fixed for the unit)
-    int ph_lo = 0, ph_hi = pl.W;
-    if (p.packed)
-      packed_phase(pl.W, (int)gridDim.x, un.b * p.Hkv + un.hkv, un.w, &ph_lo, &ph_hi);
-    const bool split = p.packed && (ph_hi - ph_lo) != pl.W;
     const int nseg = sched_segments(pl.sched, p.causal);
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
@@ -519,18 +590,6 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
           int *sem = p.sem + tile_idx;
-          int rank;
-          if (!split) {  // the head's workers share one round: plain shift order
-            rank = dq_rank(pl.sched, p.causal, p.N, q, kv);
-          } else if (!p.causal) {
-            rank = packed_rank(0, p.N, (int)gridDim.x, un.b * p.Hkv + un.hkv, q, kv);
-          } else {  // count the phase's earlier contributions, a slice per lane
-            const int per = (ph_hi - ph_lo + 31) >> 5;
-            const int cb = ph_lo + lane * per;
-            const int ce = cb + per < ph_hi ? cb + per : ph_hi;
-            const int n = cb < ce ? packed_count_in_phase(1, p.N, q, kv, cb, ce) : 0;
-            rank = packed_count_before(1, p.N, q, ph_lo) + (int)__reduce_add_sync(0xffffffffu, n);
-          }
           if (!agree(et == 0 ? mbar_wait(bar.g5_done, it & 1, ab) : true)) {
             ok = false;
             break;
@@ -546,9 +605,9 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           __syncwarp();
           if (lane == 0) mbar_arrive(bar.dq_empty);
           if (et == 0) DASH_TRACE(p, 15);
-          // the semaphore counts the epilogue threads that have finished a partial: the
-          // contributor of rank r goes once all 128 threads of rank r-1 have released
-          if (DET && !agree(et == 0 ? sem_wait(sem, rank * 128, ab) : true)) {
+          // the semaphore counts the partials added so far: the contributor of rank r goes
+          // once rank r-1 has released it; the poller warp has been watching it
+          if (DET && !agree(et == 0 ? counter_wait(seen, it + 1, ab) : true)) {
             ok = false;
             break;
           }
@@ -564,7 +623,10 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
                          __uint_as_float(v[ch][4 * j + 3]));
             }
           }
-          if (DET) red_release_add(sem, 1);  // after this thread's reductions
+          if (DET) {  // one release for the warpgroup, after all of its reductions
+            named_bar_sync(1, 128);
+            if (et == 0) red_release_add(sem, 1);
+          }
           if (et == 0) DASH_TRACE(p, 17);
         }
       }
@@ -643,6 +705,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar.dkv_empty, 4);
     mbar_init(bar.drain, 1);
     *s_abort = 0;
+    *reinterpret_cast<uint32_t *>(smem + L::offMisc + 16) = 0;  // semaphores acquired
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -664,6 +727,7 @@ __global__ void __launch_bounds__(512, 1)
     regs_set<RegSplit<D>::kCtl, RegSplit<D>::kLaunch>();
     if (warp == 0) bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
     if (warp == 1) bwd_mma<D>(p, smem, tmem, bar, ab);
+    if (DET && warp == 3) bwd_sem_poller<D>(p, smem, ab);
   } else if (warp < 12) {
     regs_set<RegSplit<D>::kSoftmax, RegSplit<D>::kLaunch>();
     bwd_softmax_grad<D>(p, smem, tmem, bar, ab);
