@@ -115,6 +115,7 @@ BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
 
 #ifdef DASH_TRACE_BUILD
 unsigned long long *g_trace = nullptr;  // development trace build only
+int g_trace_cta = 0;
 #endif
 
 // How the backward tile kernel's grid is used: the workers of all heads, head-major, dealt
@@ -258,8 +259,10 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   p.scale = sc;
 #ifdef DASH_TRACE_BUILD
   p.trace = g_trace;
+  p.trace_cta = g_trace_cta;
 #else
   p.trace = nullptr;
+  p.trace_cta = 0;
 #endif
   if ((stages & DASH_BWD_TILES) &&
       dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC, tq, tk, tv, tdo, p, plan.grid, s) !=
@@ -313,8 +316,12 @@ const char *dash_status_string(dash_status_t s) {
 }
 
 #ifdef DASH_TRACE_BUILD
-// Development trace build only: device buffer of 64 x 32 u64 for CTA 0's event clocks.
-void dash_debug_set_trace(unsigned long long *buf) { g_trace = buf; }
+// Development trace build only: device buffer of 64 x 32 u64 for the event clocks of CTA
+// `cta`.
+void dash_debug_set_trace(unsigned long long *buf, int cta) {
+  g_trace = buf;
+  g_trace_cta = cta;
+}
 #endif
 
 // ------------------------------------------------------------------ schedule queries

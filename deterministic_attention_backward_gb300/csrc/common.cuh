@@ -40,15 +40,16 @@ struct BwdParams {
   float scale_log2; // scale * log2(e)
   float scale;
   unsigned long long *trace;  // development trace build only: [64 steps][32 events] clock64
+  int trace_cta;              // development trace build only: the CTA whose events are kept
 };
 
 // Development trace build (compiled with -DDASH_TRACE_BUILD into a separate library): the
-// roles of CTA 0 record clock64() at fixed events of their first 64 steps, indexed by the
+// roles of one CTA record clock64() at fixed events of their first 64 steps, indexed by the
 // role's own step counter `it`.  In the product build the macro expands to nothing.
 #ifdef DASH_TRACE_BUILD
 #define DASH_TRACE(p, slot)                                              \
   do {                                                                   \
-    if ((p).trace && blockIdx.x == 0 && it < 64u)                        \
+    if ((p).trace && (int)blockIdx.x == (p).trace_cta && it < 64u)       \
       (p).trace[it * 32u + (slot)] = (unsigned long long)clock64();      \
   } while (0)
 #else
