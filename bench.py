@@ -157,6 +157,22 @@ class Clocks:
 
 
 # ------------------------------------------------------------------------------ GPU arm
+def slowest_rank_ms(elapsed_ms, world, device):
+    """The timed region's length on the slowest rank (every rank gets the same value)."""
+    if world <= 1:
+        return elapsed_ms
+    import torch
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(step_flops, steps, world, elapsed_ms):
+    """Whole-job throughput: the work of every rank (each runs the full workload) over the
+    slowest rank's time."""
+    return step_flops * steps * world / (elapsed_ms / 1e3) / 1e12
+
+
 def run_gpu(args, wl, rank, world):
     import torch
     import deterministic_attention_backward_gb300 as dash
@@ -228,10 +244,7 @@ def run_gpu(args, wl, rank, world):
     tile_ms = sum(a.elapsed_time(b) for a, b in evs)
     for p in probs:
         dash.status(p["ws"])
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = slowest_rank_ms(elapsed_ms, world, dev)
 
     if args.quick:  # timed loop only (profiling runs)
         return {"value_tflops": round(step_flops * args.steps / (elapsed_ms / 1e3) / 1e12, 2),
@@ -296,7 +309,7 @@ def run_gpu(args, wl, rank, world):
         e2e_val = step_flops * n_e2e / (a.elapsed_time(b) / 1e3) / 1e12 * world
 
     peak, peak_sus, peak_kind = peaks()
-    value = step_flops * args.steps * world / (elapsed_ms / 1e3) / 1e12
+    value = job_tflops(step_flops, args.steps, world, elapsed_ms)
     tile_tflops = step_flops * args.steps / (tile_ms / 1e3) / 1e12
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
