@@ -56,9 +56,15 @@
 namespace dash {
 namespace {
 
-template <int D>
+template <int D, bool DET>
 struct BwdLayout {
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kStages = (D == 64) ? (DET ? 4 : 3) : 2;
+  // D = 64, atomic variant: the dQ partial goes out by one bulk (TMA) reduction from a
+  // shared-memory staging tile instead of 2048 vector reductions per step.  At D = 128 there
+  // is no room for the staging tile.  The ordered variant keeps the vector reductions: a
+  // bulk reduction's completion (needed before the semaphore release) arrives more than a
+  // step later, longer than the one-step gap between a dQ tile's contributors.
+  static constexpr bool kBulkDQ = (D == 64 && !DET);
   static constexpr int kTileBytes = D * kTile * 2;  // one [128 x D] bf16 tile
   static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kStageBytes = 2 * kTileBytes;  // Q_i and dO_i
@@ -67,7 +73,9 @@ struct BwdLayout {
   static constexpr int offStage = 2 * kTileBytes;  // stage s: Q at +s*kStageBytes, dO after
   static constexpr int offDS = offStage + kStages * kStageBytes;
   static constexpr int kDSBytes = kTile * kTile * 2;
-  static constexpr int offLSE = offDS + kDSBytes;
+  static constexpr int offStg = offDS + kDSBytes;  // fp32 dQ partial, tile-native layout
+  static constexpr int kStgBytes = kBulkDQ ? kTile * D * 4 : 0;
+  static constexpr int offLSE = offStg + kStgBytes;
   static constexpr int offDVEC = offLSE + kStages * kTile * 4;
   static constexpr int offBar = offDVEC + kStages * kTile * 4;
   static constexpr int kNumBars = 2 * kStages + 15;
@@ -129,12 +137,12 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams &p, const Plan &pl, 
   return r;
 }
 
-template <int D>
+template <int D, bool DET>
 struct Bars {
   uint64_t *full, *empty, *kv_full, *kv_empty, *s_full, *s_free, *dp_full, *pds, *g5_done,
       *dq_empty, *dkv_full, *dkv_empty, *drain;
   __device__ explicit Bars(uint8_t *smem) {
-    using L = BwdLayout<D>;
+    using L = BwdLayout<D, DET>;
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + L::offBar);
     full = b;
     empty = b + L::kStages;
@@ -155,11 +163,11 @@ struct Bars {
 
 // ---------------------------------------------------------------------------------------
 // TMA producer: the whole warp runs the loop; one elected lane issues the copies.
-template <int D>
+template <int D, bool DET>
 __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                              const CUtensorMap *tdo, const BwdParams &p, uint8_t *smem,
-                             const Bars<D> &bar, const Abort &ab) {
-  using L = BwdLayout<D>;
+                             const Bars<D, DET> &bar, const Abort &ab) {
+  using L = BwdLayout<D, DET>;
   uint32_t it = 0, seg_it = 0;
   int last_full[L::kStages];
 #pragma unroll
@@ -237,10 +245,10 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
 // warp-uniform); one elected lane issues each tcgen05 instruction.  Within a segment the
 // S^T product of the next step is issued as soon as the softmax-gradient warps have read
 // the current S^T, so it runs while they compute P and dS.
-template <int D>
-__device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D> &bar,
+template <int D, bool DET>
+__device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
                         const Abort &ab) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, DET>;
   constexpr uint32_t kIdescSS = make_idesc_bf16(128, 128, false, false);  // G1, G2
   constexpr uint32_t kIdescTS = make_idesc_bf16(128, D, false, true);     // G3x, G4x
   constexpr uint32_t kIdescG5 = make_idesc_bf16(128, D, true, true);      // G5
@@ -376,10 +384,10 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
 // read S^T and release its columns at once, compute P^T in registers, then, when dP^T has
 // arrived, compute dS^T = P^T (dP^T - Dvec) chunk by chunk and write P^T and dS^T (bf16x2)
 // back over the dP^T columns just read; dS also goes to shared memory for G5.
-template <int D>
+template <int D, bool DET>
 __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tmem,
-                                 const Bars<D> &bar, const Abort &ab) {
-  using L = BwdLayout<D>;
+                                 const Bars<D, DET> &bar, const Abort &ab) {
+  using L = BwdLayout<D, DET>;
   const int warp = warp_id(), lane = lane_id();
   const int x = (warp - 4) >> 2;  // query half: columns [64x, 64x + 64)
   const int quad = warp & 3;
@@ -534,9 +542,9 @@ __device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, con
 // L2 round trips of the polling thus overlap the computation of the dQ partial instead
 // of following its drain.  It runs ahead of the epilogue by any number of steps; that is
 // safe because a tile's count only grows.
-template <int D>
+template <int D, bool DET>
 __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &ab) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, DET>;
   const int lane = lane_id();
   uint32_t *seen = reinterpret_cast<uint32_t *>(smem + L::offMisc + 16);
   uint32_t it = 0;
@@ -567,9 +575,9 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
 }
 
 template <int D, bool DET>
-__device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D> &bar,
+__device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
                              const Abort &ab) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, DET>;
   const int warp = warp_id(), lane = lane_id();
   const int et = threadIdx.x - 12 * 32;  // 0..127
   const int quad = warp & 3;
@@ -586,6 +594,7 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
     return decision[dec++ & 1] != 0;
   };
   const uint32_t *seen = reinterpret_cast<const uint32_t *>(smem + L::offMisc + 16);
+  constexpr bool kBulk = L::kBulkDQ && !DET;
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
@@ -614,6 +623,30 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           __syncwarp();
           if (lane == 0) mbar_arrive(bar.dq_empty);
           if (et == 0) DASH_TRACE(p, 15);
+          float *tile = p.dqacc + tile_idx * (size_t)(kTile * D);
+          if constexpr (kBulk) {
+            // the partial into the staging tile (same tile-native layout as the accumulator;
+            // the previous reduction finished reading it before thread 0 left the last step)
+            float4 *stg = reinterpret_cast<float4 *>(smem + L::offStg);
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                stg[(ch * 8 + j) * kTile + r] =
+                    make_float4(__uint_as_float(v[ch][4 * j]), __uint_as_float(v[ch][4 * j + 1]),
+                                __uint_as_float(v[ch][4 * j + 2]), __uint_as_float(v[ch][4 * j + 3]));
+            }
+            fence_proxy_async_smem();
+            // every row staged: one thread adds the whole tile with a single bulk reduction
+            named_bar_sync(1, 128);
+            if (et == 0) {
+              DASH_TRACE(p, 16);
+              bulk_reduce_add_f32(tile, stg, kTile * D * 4);
+              bulk_wait_read();
+              DASH_TRACE(p, 17);
+            }
+            continue;
+          }
           // the semaphore counts the partials added so far: the contributor of rank r goes
           // once rank r-1 has released it; the poller warp has been watching it
           if (DET && !agree(et == 0 ? counter_wait(seen, it + 1, ab) : true)) {
@@ -621,7 +654,6 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
             break;
           }
           if (et == 0) DASH_TRACE(p, 16);
-          float *tile = p.dqacc + tile_idx * (size_t)(kTile * D);
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
 #pragma unroll
@@ -678,6 +710,8 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
       ++seg_it;
     }
   }
+  // leave no bulk reduction in flight
+  if (kBulk && et == 0) bulk_wait_done();
 }
 
 // ---------------------------------------------------------------------------------------
@@ -686,13 +720,13 @@ __global__ void __launch_bounds__(512, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const BwdParams p) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, DET>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(p.status, kErrSmemAlign);
     return;
   }
-  const Bars<D> bar(smem);
+  const Bars<D, DET> bar(smem);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L::offMisc);
   int *s_abort = reinterpret_cast<int *>(smem + L::offMisc + 4);
   const Abort ab{s_abort, p.status};
@@ -736,12 +770,12 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp < 4) {
     regs_set<RegSplit<D>::kCtl, RegSplit<D>::kLaunch>();
-    if (warp == 0) bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
-    if (warp == 1) bwd_mma<D>(p, smem, tmem, bar, ab);
-    if (DET && warp == 3) bwd_sem_poller<D>(p, smem, ab);
+    if (warp == 0) bwd_producer<D, DET>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
+    if (warp == 1) bwd_mma<D, DET>(p, smem, tmem, bar, ab);
+    if (DET && warp == 3) bwd_sem_poller<D, DET>(p, smem, ab);
   } else if (warp < 12) {
     regs_set<RegSplit<D>::kSoftmax, RegSplit<D>::kLaunch>();
-    bwd_softmax_grad<D>(p, smem, tmem, bar, ab);
+    bwd_softmax_grad<D, DET>(p, smem, tmem, bar, ab);
   } else {
     regs_set<RegSplit<D>::kEpi, RegSplit<D>::kLaunch>();
     bwd_epilogue<D, DET>(p, smem, tmem, bar, ab);
@@ -758,7 +792,7 @@ __global__ void __launch_bounds__(512, 1)
 template <int D, bool DET>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &tdo, const BwdParams &p, int grid, cudaStream_t stream) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, DET>;
   auto kern = bwd_kernel<D, DET>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
@@ -773,8 +807,9 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 }  // namespace
 
-size_t bwd_smem_bytes(int D) {
-  return D == 64 ? BwdLayout<64>::kBytes : BwdLayout<128>::kBytes;
+size_t bwd_smem_bytes(int D, bool deterministic) {
+  if (D == 64) return deterministic ? BwdLayout<64, true>::kBytes : BwdLayout<64, false>::kBytes;
+  return deterministic ? BwdLayout<128, true>::kBytes : BwdLayout<128, false>::kBytes;
 }
 
 cudaError_t launch_bwd(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -151,6 +151,23 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Bulk (TMA) reduction of `bytes` fp32 values from shared memory into global memory
+// (element-wise add, performed in L2), tracked by this thread's bulk async-group.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *dst, const void *src, uint32_t bytes) {
+  asm volatile(
+      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+      "r"(smem_u32(src)), "r"(bytes)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until this thread's bulk groups have finished reading their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until this thread's bulk groups are complete (their global writes performed).
+__device__ __forceinline__ void bulk_wait_done() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor cores, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
