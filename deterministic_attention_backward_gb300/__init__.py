@@ -19,18 +19,18 @@ import os
 import threading
 
 __all__ = ["fwd", "bwd", "bwd_workspace_bytes", "fwd_workspace_bytes", "status",
-           "sched_table", "sched_grid", "packed_rank", "SCHEDULES", "lib", "DashError"]
+           "sched_table", "sched_grid", "sched_resolve", "packed_rank", "SCHEDULES", "lib", "DashError"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdash_attn.so")
 
-SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3, "shift_fill": 4}
+SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3, "shift_fill": 4, "auto": 5}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "device-side wait timed out", 5: "workspace missing or too small"}
 EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_workspace_bytes",
            "dash_attn_bwd", "dash_attn_bwd_stages", "dash_attn_status",
            "dash_status_string", "dash_sched_workers", "dash_sched_segments", "dash_sched_steps",
-           "dash_sched_step", "dash_sched_grid", "dash_sched_packed_rank",
+           "dash_sched_step", "dash_sched_grid", "dash_sched_packed_rank", "dash_sched_resolve",
            "dash_attn_bwd_noalloc"]
 
 
@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.dash_sched_grid.restype = i
         L.dash_sched_packed_rank.argtypes = [i, i, i, i, i, i, i]
         L.dash_sched_packed_rank.restype = i
+        L.dash_sched_resolve.argtypes = [i, i, i]
+        L.dash_sched_resolve.restype = i
         _lib = L
         return L
 
@@ -165,7 +167,8 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, schedule: str = "shift",
         check: bool = False, stages: int = ALL_STAGES):
     """Attention backward: returns (dQ, dK, dV) bf16.  ``schedule`` is one of
     ``atomic`` (non-deterministic reference), ``serial``, ``descending``, ``shift``,
-    ``shift_fill`` (packed shift: all SMs busy, heads split across rounds run in phases).
+    ``shift_fill`` (packed shift: all SMs busy, heads split across rounds run in phases),
+    ``auto`` (the measured-fastest deterministic schedule, see ``sched_resolve``).
     ``stages`` (PROLOGUE | TILES | EPILOGUE) launches only part of the work, in order, on
     the same workspace (for timing the tile kernel on its own)."""
     import torch
@@ -197,6 +200,14 @@ def status(workspace, stream=None):
     """Synchronise and raise DashError if the last call on ``workspace`` reported a
     device-side failure (a bounded wait that ran out)."""
     _check(lib().dash_attn_status(workspace.data_ptr(), _stream_ptr(stream)), "device status")
+
+
+def sched_resolve(schedule: str, causal: bool, N: int) -> str:
+    """The schedule the backward runs for ``schedule`` (``auto`` resolved) at N tiles."""
+    r = lib().dash_sched_resolve(SCHEDULES[schedule], int(bool(causal)), N)
+    if r < 0:
+        raise ValueError("unsupported schedule arguments")
+    return {v: k for k, v in SCHEDULES.items()}[r]
 
 
 def sched_grid(schedule: str, causal: bool, N: int, heads: int, sms: int) -> int:

@@ -124,6 +124,13 @@ struct LaunchPlan {
   int sched, workers, grid, packed;
 };
 
+// DASH_SCHED_AUTO: SHIFT_FILL where a shift schedule exists, DESCENDING for a causal mask
+// with an odd tile count (the measured choice; see the header).
+int resolve_sched(int sched, int mask, int N) {
+  if (sched != DASH_SCHED_AUTO) return sched;
+  return (mask == DASH_MASK_CAUSAL && (N % 2)) ? DASH_SCHED_DESCENDING : DASH_SCHED_SHIFT_FILL;
+}
+
 // False when a shift schedule cannot have every worker of a head resident at once.
 bool make_plan(int sched, int causal, int N, int heads, int sms, LaunchPlan *pl) {
   pl->sched = dash::traversal(sched, causal, N);
@@ -199,7 +206,8 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   dash_status_t st = check_sizes(B, S, H, group, D);
   if (st != DASH_OK) return st;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
-  if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_SHIFT_FILL) return DASH_ERR_INVALID;
+  if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_AUTO) return DASH_ERR_INVALID;
+  sched = (dash_sched_t)resolve_sched(sched, mask, S / kTile);
   const void *ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
   for (const void *ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return DASH_ERR_INVALID;
@@ -325,11 +333,17 @@ void dash_debug_set_trace(unsigned long long *buf, int cta) {
 #endif
 
 // ------------------------------------------------------------------ schedule queries
-static bool sched_args_ok(int sched, int mask, int N) {
-  if (sched < 0 || sched > 4 || (mask != 0 && mask != 1) || N <= 0) return false;
+static bool sched_args_ok(int &sched, int mask, int N) {
+  if (sched < 0 || sched > DASH_SCHED_AUTO || (mask != 0 && mask != 1) || N <= 0) return false;
+  sched = resolve_sched(sched, mask, N);
   if ((sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL) && mask == 1 && (N % 2))
     return false;
   return true;
+}
+
+int dash_sched_resolve(int sched, int mask, int N) {
+  if (!sched_args_ok(sched, mask, N)) return -1;
+  return sched;
 }
 
 int dash_sched_grid(int sched, int mask, int N, int heads, int sms) {
@@ -341,7 +355,8 @@ int dash_sched_grid(int sched, int mask, int N, int heads, int sms) {
 }
 
 int dash_sched_packed_rank(int mask, int N, int heads, int grid, int head, int q, int kv) {
-  if (!sched_args_ok(DASH_SCHED_SHIFT_FILL, mask, N) || heads <= 0 || head < 0 ||
+  int fill = DASH_SCHED_SHIFT_FILL;
+  if (!sched_args_ok(fill, mask, N) || heads <= 0 || head < 0 ||
       head >= heads || q < 0 || q >= N || kv < 0 || kv >= N || (mask && kv > q))
     return -1;
   const int W = dash::sched_workers(dash::kShift, mask, N);
@@ -355,12 +370,14 @@ int dash_sched_workers(int sched, int mask, int N) {
 }
 
 int dash_sched_segments(int sched, int mask, int N, int worker) {
+  sched = resolve_sched(sched, mask, N);
   const int W = dash_sched_workers(sched, mask, N);
   if (W < 0 || worker < 0 || worker >= W) return -1;
   return dash::sched_segments(dash::traversal(sched, mask, N), mask);
 }
 
 int dash_sched_steps(int sched, int mask, int N, int worker, int segment) {
+  sched = resolve_sched(sched, mask, N);
   const int nseg = dash_sched_segments(sched, mask, N, worker);
   if (nseg < 0 || segment < 0 || segment >= nseg) return -1;
   return dash::seg_steps(dash::traversal(sched, mask, N), mask, N, worker, segment);
@@ -368,6 +385,7 @@ int dash_sched_steps(int sched, int mask, int N, int worker, int segment) {
 
 int dash_sched_step(int sched, int mask, int N, int worker, int segment, int step, int *kv,
                     int *q, int *rank) {
+  sched = resolve_sched(sched, mask, N);
   const int n = dash_sched_steps(sched, mask, N, worker, segment);
   if (n < 0 || step < 0 || step >= n) return -1;
   const int t = dash::traversal(sched, mask, N);

@@ -75,13 +75,22 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           exactly the DASH_SCHED_SHIFT order.  Keeps every SM busy where
  *                           plain SHIFT leaves SMs waiting for a head's remaining workers.
  *                           Deterministic for a given SM count (dash_sched_grid,
- *                           dash_sched_packed_rank give the order). */
+ *                           dash_sched_packed_rank give the order).
+ *  DASH_SCHED_AUTO       -- the deterministic schedule that measured fastest on GB300 for
+ *                           the mask and tile count (dash_sched_resolve names it): the pages
+ *                           leave the choice to the user.  Measured over every configuration
+ *                           of the benchmark (full and causal masks, D = 64 and 128,
+ *                           S = 512 .. 16384, GQA 4:1), SHIFT_FILL is the fastest or within
+ *                           1 % of it wherever a shift schedule exists; for a causal mask
+ *                           with an odd tile count (no Symmetric Shift) DESCENDING beats
+ *                           SERIAL.  So AUTO = SHIFT_FILL, or DESCENDING for causal odd N. */
 typedef enum {
   DASH_SCHED_ATOMIC = 0,
   DASH_SCHED_SERIAL = 1,
   DASH_SCHED_DESCENDING = 2,
   DASH_SCHED_SHIFT = 3,
-  DASH_SCHED_SHIFT_FILL = 4
+  DASH_SCHED_SHIFT_FILL = 4,
+  DASH_SCHED_AUTO = 5
 } dash_sched_t;
 
 typedef enum {
@@ -193,6 +202,9 @@ const char *dash_status_string(dash_status_t status);
  * tile *q with KV block *kv, and its dQ partial is the rank-th addition into tile q.
  * Return -1 on unsupported arguments. */
 int dash_sched_workers(int sched, int mask, int N);
+/* The schedule dash_attn_bwd runs for `sched` (DASH_SCHED_AUTO resolved, every other value
+ * returned unchanged) with `mask` and N = S/128 tiles; -1 on bad arguments. */
+int dash_sched_resolve(int sched, int mask, int N);
 /* Number of CTAs dash_attn_bwd launches for its tile kernel on a GPU with `sms` SMs, for
  * `heads` = B * H/group (batch, kv head) pairs; -1 where dash_attn_bwd would reject the
  * schedule arguments (e.g. a shift schedule whose workers per head exceed the SMs). */

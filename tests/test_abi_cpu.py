@@ -127,3 +127,17 @@ def test_schedule_query_rejects_bad_arguments(L):
     assert L.dash_sched_workers(3, 1, 5) == -1
     assert L.dash_sched_workers(7, 0, 4) == -1
     assert L.dash_sched_step(1, 0, 4, 0, 0, 4, None, None, None) == -1
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_auto_schedule_resolution(L, causal, N):
+    """AUTO runs the packed shift schedule wherever a shift schedule exists, Descending
+    Q-Tile Iteration for a causal mask with an odd tile count; other schedules pass through."""
+    want = "descending" if (causal and N % 2) else "shift_fill"
+    assert dash.sched_resolve("auto", causal, N) == want
+    for name in ("atomic", "serial", "descending"):
+        assert dash.sched_resolve(name, causal, N) == name
+    assert dash.sched_table("auto", causal, N) == dash.sched_table(want, causal, N)
+    assert dash.sched_grid("auto", causal, N, 64, 152) == dash.sched_grid(want, causal, N, 64, 152)
+    assert L.dash_sched_resolve(6, int(causal), N) == -1

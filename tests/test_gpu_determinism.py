@@ -99,3 +99,15 @@ def test_every_partial_takes_its_turn(dash, shape, causal):
         p.dash.status(p.ws)
         sem = p.semaphores().cpu().numpy()
         assert (sem == want[None, None, :]).all(), sched
+
+
+@pytest.mark.parametrize("shape,causal", [((2, 1024, 4, 2, 128), False), ((2, 1024, 4, 2, 128), True),
+                                          ((1, 384, 2, 2, 64), True)])
+def test_auto_runs_the_resolved_schedule(dash, shape, causal):
+    p = Problem(dash, *shape, causal, seed=3)
+    want = dash.sched_resolve("auto", causal, shape[1] // 128)
+    ref = snapshot(p.run(want))
+    out = p.run("auto")
+    p.dash.status(p.ws)
+    for a, b in zip(out, ref):
+        assert torch.equal(a, b), want
