@@ -24,12 +24,14 @@
 // Pipeline (MMA issue order; every hand-off is an mbarrier):
 //   segment start: G1(first) -> s_full
 //   each step t:   [dQ(t-1) drained] G2(t) -> dp_full,
-//                  [S^T(t) read] G1(t+1) -> s_full        (within the segment)
-//                  [P/dS half a] G3a G4a, [half b] G3b G4b -> stage free,
+//                  [P^T(t) written] G3(t), G1(t+1) -> s_full   (G1 within the segment)
+//                  [dS half a] G4a, [half b] G4b -> stage free,
 //                  G5(t) -> g5_done
-// The softmax-gradient warpgroups read S^T(t) and release its columns at once, so G1(t+1)
-// runs while they compute P and dS; they write P^T and dS^T over the dP^T columns they have
-// just read.  The epilogue copies the dQ partial to registers first and waits for its
+// The softmax-gradient warpgroups read S^T(t), compute P and write P^T (bf16) over the
+// first half of the S^T columns they read, so G3(t) and then G1(t+1) run on the tensor pipe
+// while they compute dS; they write dS^T over the dP^T columns they have just read, and only
+// G4 and G5 remain between dS and the next step.  The epilogue copies the dQ partial to
+// registers first and waits for its
 // turn on the semaphore afterwards, so a waiting reduction does not hold tensor memory.
 // The semaphore of a dQ tile counts the partials added to it; a poller warp watches the
 // semaphores of this CTA's coming steps ahead of time, so the epilogue usually finds its
@@ -47,7 +49,7 @@
 //               [64w, 64w+64) of the tile, thread = KV row (TMEM lane)
 //   warps 12-15 epilogue warpgroup: dQ partial TMEM -> ordered/atomic fp32 reduction in
 //               global memory; dK/dV TMEM -> bf16 at the end of each segment
-// TMEM columns: S^T [0,128), dP^T then P^T/dS^T [128,256), dK [256,256+D), dV [256+D,256+2D);
+// TMEM columns: S^T then P^T [0,128), dP^T then dS^T [128,256), dK [256,256+D), dV [256+D,256+2D);
 // the dQ partial reuses [128,256) at D=128 and has its own columns [384,448) at D=64.
 #include "common.cuh"
 #include "ptx.cuh"
@@ -139,7 +141,7 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams &p, const Plan &pl, 
 
 template <int D, bool DET>
 struct Bars {
-  uint64_t *full, *empty, *kv_full, *kv_empty, *s_full, *s_free, *dp_full, *pds, *g5_done,
+  uint64_t *full, *empty, *kv_full, *kv_empty, *s_full, *p_ready, *dp_full, *pds, *g5_done,
       *dq_empty, *dkv_full, *dkv_empty, *drain;
   __device__ explicit Bars(uint8_t *smem) {
     using L = BwdLayout<D, DET>;
@@ -150,7 +152,7 @@ struct Bars {
     kv_full = b + 0;
     kv_empty = b + 1;
     s_full = b + 2;   // S^T in TMEM (MMA commit)
-    s_free = b + 3;   // S^T read by both softmax-gradient warpgroups (8 warps)
+    p_ready = b + 3;  // P^T written over S^T by both softmax-gradient warpgroups (8 warps)
     dp_full = b + 4;  // dP^T in TMEM (MMA commit)
     pds = b + 6;      // [2]: P^T, dS^T of half x in TMEM, dS in shared memory (4 warps)
     g5_done = b + 10;
@@ -278,9 +280,9 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
     const int nseg = sched_segments(pl.sched, p.causal);
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg) * p.G;
-      // segment prologue: new K_j/V_j, the S^T columns free, G1 of the first step
+      // segment prologue: new K_j/V_j and G1 of the first step (the previous step's G3,
+      // the last reader of the S^T columns, was issued before and runs first)
       if (!mbar_wait_warp(bar.kv_full, seg_it & 1, ab) ||
-          (it > 0 && !mbar_wait_warp(bar.s_free, (it - 1) & 1, ab)) ||
           !mbar_wait_warp(&bar.full[it % L::kStages], (it / L::kStages) & 1, ab)) {
         ok = false;
         break;
@@ -310,28 +312,32 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
         }
         mma_commit_e(bar.dp_full);
         DASH_TRACE(p, 1);
-        // G1 of the next step of this segment, once S^T has been read and Q_{i'} has landed
+        const bool fresh = (st == 0);  // first step of a segment starts dK/dV from zero
+        // G3: dV_j += P^T dO_i, as soon as both warpgroups have put P^T (bf16x2) over the
+        // first 32 of their 64 S^T columns; it runs while they compute dS
+        if (!mbar_wait_warp(bar.p_ready, par, ab) ||
+            (fresh && seg_it > 0 && !mbar_wait_warp(bar.dkv_empty, (seg_it - 1) & 1, ab))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts_e(tmem + L::tDV, tmem + L::tS + 64 * (k >> 2) + 8 * (k & 3),
+                   desc_of(loDOmn + ((k * 2048) >> 4)), kIdescTS, (fresh && k == 0) ? 0u : 1u);
+        DASH_TRACE(p, 2);
+        // G1 of the next step of this segment, once Q_{i'} has landed (G3 above read the
+        // S^T columns first: the tensor pipe runs a CTA's MMAs in issue order)
         if (st + 1 < nsteps) {
-          if (!mbar_wait_warp(bar.s_free, par, ab) ||
-              !mbar_wait_warp(&bar.full[(it + 1) % L::kStages], ((it + 1) / L::kStages) & 1, ab)) {
+          if (!mbar_wait_warp(&bar.full[(it + 1) % L::kStages], ((it + 1) / L::kStages) & 1, ab)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_g1(it + 1);
-          DASH_TRACE(p, 2);
         }
-        const bool fresh = (st == 0);  // first step of a segment starts dK/dV from zero
-        if (fresh && seg_it > 0) {     // previous segment's dK/dV must have been read out
-          if (!mbar_wait_warp(bar.dkv_empty, (seg_it - 1) & 1, ab)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        // G3x: dV_j += P^T dO_i and G4x: dK_j += dS^T Q_i over query half x, once warpgroup x
-        // has put P^T and dS^T of its half into the dP^T columns: within the 32-column chunk
-        // c of the half, P^T packed (bf16x2) in the first 16 columns, dS^T in the next 16.
+        // G4x: dK_j += dS^T Q_i over query half x, once warpgroup x has put dS^T of its half
+        // into the dP^T columns: within the 32-column chunk c of the half, in columns 16..31
 #pragma unroll 1
         for (int x = 0; x < 2; ++x) {
           if (!mbar_wait_warp(&bar.pds[x], par, ab)) {
@@ -342,12 +348,9 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
           DASH_TRACE(p, 3 + x);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t acol = L::tDP + 64 * x + 32 * (k >> 1) + 8 * (k & 1);
-            const uint32_t acc = (fresh && x == 0 && k == 0) ? 0u : 1u;
-            mma_ts_e(tmem + L::tDV, tmem + acol, desc_of(loDOmn + (((4 * x + k) * 2048) >> 4)),
-                     kIdescTS, acc);
-            mma_ts_e(tmem + L::tDK, tmem + acol + 16, desc_of(loQmn + (((4 * x + k) * 2048) >> 4)),
-                     kIdescTS, acc);
+            const uint32_t acol = L::tDP + 64 * x + 32 * (k >> 1) + 8 * (k & 1) + 16;
+            mma_ts_e(tmem + L::tDK, tmem + acol, desc_of(loQmn + (((4 * x + k) * 2048) >> 4)),
+                     kIdescTS, (fresh && x == 0 && k == 0) ? 0u : 1u);
           }
         }
         if (!ok) break;
@@ -381,9 +384,10 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
 
 // ---------------------------------------------------------------------------------------
 // Softmax-gradient warpgroup x (query columns [64x, 64x+64) of the tile; thread = KV row):
-// read S^T and release its columns at once, compute P^T in registers, then, when dP^T has
-// arrived, compute dS^T = P^T (dP^T - Dvec) chunk by chunk and write P^T and dS^T (bf16x2)
-// back over the dP^T columns just read; dS also goes to shared memory for G5.
+// read S^T, compute P^T in registers and write it (bf16x2) over the first 32 of the S^T
+// columns just read (the A operand of G3); then, when dP^T has arrived, compute
+// dS^T = P^T (dP^T - Dvec) chunk by chunk and write it (bf16x2) back over the dP^T columns
+// just read; dS also goes to shared memory for G5.
 template <int D, bool DET>
 __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tmem,
                                  const Bars<D, DET> &bar, const Abort &ab) {
@@ -425,9 +429,6 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
             tmem_ld32(tmem + lane_off + L::tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
             tmem_ld32(tmem + lane_off + L::tS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
             tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar.s_free);  // S^T columns may be overwritten now
             if (lane == 0 && warp == 4 + 4 * x) DASH_TRACE(p, 6 + 4 * x);
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
@@ -443,6 +444,14 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
               pk[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
             }
           }
+          // P^T (bf16x2) over the first 32 of this half's S^T columns, all read above: the
+          // A operand of G3, which then runs while dS is computed
+          tmem_st16(tmem + lane_off + L::tS + c0, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+          tmem_st16(tmem + lane_off + L::tS + c0 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar.p_ready);
           if (lane == 0 && warp == 4 + 4 * x) DASH_TRACE(p, 7 + 4 * x);
           // Dvec of the first chunk into registers while dP^T is still being computed
           float dv[32];
@@ -476,8 +485,7 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
                     *reinterpret_cast<const float4 *>(dvec_s + c0 + 32 + c);
             }
             if (lane == 0 && warp == 4) DASH_TRACE(p, 19 + 4 * ch);
-            // both into the chunk's own (already read) dP^T columns: P^T, then dS^T
-            tmem_st16(tmem + lane_off + col, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * ch]));
+            // dS^T into columns 16..31 of the chunk's own (already read) dP^T columns
             tmem_st16(tmem + lane_off + col + 16, dk);
             if (lane == 0 && warp == 4) DASH_TRACE(p, 20 + 4 * ch);
             // dS into shared memory as the MN-major A operand of G5: row r of box x,
@@ -740,7 +748,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar.kv_full, 1);
     mbar_init(bar.kv_empty, 1);
     mbar_init(bar.s_full, 1);
-    mbar_init(bar.s_free, 8);
+    mbar_init(bar.p_ready, 8);
     mbar_init(bar.dp_full, 1);
     mbar_init(&bar.pds[0], 4);
     mbar_init(&bar.pds[1], 4);
