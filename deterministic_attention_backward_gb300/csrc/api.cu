@@ -30,16 +30,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return g_encode;
 }
 
-// [B, S, Hx, D] bf16 viewed as a 3-D tensor (D, Hx, B*S); box = 64 columns x 1 head x 128
-// rows, 128-byte swizzle: one box lands in shared memory as 128 rows of 128 bytes.
+// [B, S, Hx, D] bf16 viewed as a 4-D tensor (D, Hx, S, B); box = 64 columns x 1 head x 128
+// rows x 1 batch, 128-byte swizzle: one box lands in shared memory as 128 rows of 128 bytes.
+// Rows of a tile past S (S not a multiple of 128) are outside the tensor and read as zeros.
 bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int Hx, int D) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hx, (cuuint64_t)B * (cuuint64_t)S};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hx * D * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)dash::kBoxCols, 1, (cuuint32_t)kTile};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hx, (cuuint64_t)S, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hx * D * 2,
+                                 (cuuint64_t)S * Hx * D * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)dash::kBoxCols, 1, (cuuint32_t)kTile, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -71,15 +73,16 @@ dash_status_t device_info(DevInfo *out) {
 
 // ------------------------------------------------------------------ validation / workspace
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int tiles(int S) { return (S + kTile - 1) / kTile; }  // N: a last, partial tile counts
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 dash_status_t check_sizes(int B, int S, int H, int group, int D) {
   if (B <= 0 || S <= 0 || H <= 0 || group <= 0 || D <= 0) return DASH_ERR_INVALID;
   if (H % group) return DASH_ERR_INVALID;
   if (D != 64 && D != 128) return DASH_ERR_UNSUPPORTED;
-  if (S % kTile) return DASH_ERR_UNSUPPORTED;
   // index arithmetic inside the kernels is 32-bit for row numbers
-  if ((long long)B * S >= (1LL << 31) / 2 || (long long)B * H * (S / kTile) >= (1LL << 30))
+  if ((long long)B * tiles(S) * kTile >= (1LL << 31) / 2 ||
+      (long long)B * H * tiles(S) >= (1LL << 30))
     return DASH_ERR_UNSUPPORTED;
   return DASH_OK;
 }
@@ -93,9 +96,10 @@ struct BwdWorkspace {
   size_t dqacc_bytes, sem_bytes, total;
 };
 
+// Row arrays are per tile: S padded up to N*128 rows per (b, h).
 BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
   BwdWorkspace w{};
-  const size_t rows = (size_t)B * H * S;
+  const size_t rows = (size_t)B * H * tiles(S) * kTile;
   size_t off = 0;
   w.status = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + off);
   off += kStatusBytes;
@@ -107,7 +111,7 @@ BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
   w.dvec = reinterpret_cast<float *>(static_cast<char *>(ws) + off);
   off = align256(off + rows * 4);
   w.sem = reinterpret_cast<int *>(static_cast<char *>(ws) + off);
-  w.sem_bytes = (size_t)B * H * (S / kTile) * 4;
+  w.sem_bytes = (size_t)B * H * tiles(S) * 4;
   off = align256(off + w.sem_bytes);
   w.total = off;
   return w;
@@ -190,7 +194,7 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
   p.H = H;
   p.Hkv = Hkv;
   p.G = group;
-  p.N = S / kTile;
+  p.N = tiles(S);
   p.causal = mask == DASH_MASK_CAUSAL;
   p.scale_log2 = resolve_scale(scale, D) * dash::kLog2e;
   return dash::launch_fwd(D, tq, tk, tv, p, s) == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
@@ -207,11 +211,11 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   if (st != DASH_OK) return st;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
   if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_AUTO) return DASH_ERR_INVALID;
-  sched = (dash_sched_t)resolve_sched(sched, mask, S / kTile);
+  sched = (dash_sched_t)resolve_sched(sched, mask, tiles(S));
   const void *ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
   for (const void *ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return DASH_ERR_INVALID;
-  const int N = S / kTile;
+  const int N = tiles(S);
   const int causal = mask == DASH_MASK_CAUSAL;
   const bool shift = sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL;
   if (shift && causal && (N % 2)) return DASH_ERR_UNSUPPORTED;
@@ -237,6 +241,11 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
     // status word + dQ accumulator are contiguous; semaphores separately
     if (cudaMemsetAsync(w.status, 0, kStatusBytes + w.dqacc_bytes, s) != cudaSuccess ||
         cudaMemsetAsync(w.sem, 0, w.sem_bytes, s) != cudaSuccess)
+      return DASH_ERR_CUDA;
+    // a partial last tile: its padding rows of lse2 / Dvec must read as zero
+    if ((S % kTile) &&
+        cudaMemsetAsync(w.lse2, 0, reinterpret_cast<char *>(w.sem) - reinterpret_cast<char *>(w.lse2),
+                        s) != cudaSuccess)
       return DASH_ERR_CUDA;
     if (dash::launch_preprocess(static_cast<const __nv_bfloat16 *>(o),
                                 static_cast<const __nv_bfloat16 *>(dout), lse, w.dvec, w.lse2, B,

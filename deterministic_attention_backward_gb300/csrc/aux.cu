@@ -1,7 +1,8 @@
 // aux.cu -- the two memory-bound companions of the backward tile kernel:
 //   preprocess:  Dvec[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]   (fp32)
 //                lse2[b,h,i] = LSE[b,h,i] * log2(e)              (exp2-domain LSE)
-//   dq_convert:  dQ[b,i,h,:] = bf16_rne(scale * dQacc)            (tile-native -> BSHD)
+//                (both [B,H,N*128]: each (b,h) padded to whole tiles; padding stays zero)
+//   dq_convert:  dQ[b,i,h,:] = bf16_rne(scale * dQacc)            (tile-native -> BSHD, i < S)
 #include "common.cuh"
 
 namespace dash {
@@ -48,9 +49,10 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16 *__
       const long long bi = row / H;
       const int i = (int)(bi % S);
       const int b = (int)(bi / S);
-      const size_t r = ((size_t)b * H + h) * S + i;
+      const size_t Sp = (size_t)(S + kTile - 1) / kTile * kTile;
+      const size_t r = ((size_t)b * H + h) * Sp + i;
       dvec[r] = acc;
-      lse2[r] = lse[r] * kLog2e;
+      lse2[r] = lse[((size_t)b * H + h) * S + i] * kLog2e;
     }
   }
 }
@@ -62,7 +64,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
                                                          __nv_bfloat16 *__restrict__ dq,
                                                          float scale, int B, int S, int H) {
   constexpr int C4 = D / 4;
-  const int N = S / kTile;
+  const int N = (S + kTile - 1) / kTile;
   const long long total = (long long)B * H * N * kTile * C4;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -73,6 +75,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
     const long long bh = t / N;
     const int h = (int)(bh % H);
     const int b = (int)(bh / H);
+    if (i * kTile + r >= S) continue;  // padding rows of a partial last tile
     const float4 v = *reinterpret_cast<const float4 *>(acc + ((t * C4 + c4) * kTile + r) * 4);
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
     __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
@@ -106,7 +109,7 @@ cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
 
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B, int S,
                               int H, int D, cudaStream_t stream) {
-  const long long work = (long long)B * H * S * (D / 4);
+  const long long work = (long long)B * H * ((S + kTile - 1) / kTile) * kTile * (D / 4);
   const int grid = grid_for(work, 256, 152 * 32);
   if (D == 64)
     dq_convert_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);

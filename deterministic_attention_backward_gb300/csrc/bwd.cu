@@ -189,13 +189,13 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
       }
       if (elect_one()) {
         mbar_arrive_expect_tx(bar.kv_full, 2 * L::kTileBytes);
-        const int krow = un.b * p.S + kv * kTile;
+        // rows past S (partial last tile) are outside the tensor map and arrive as zeros
 #pragma unroll
         for (int bx = 0; bx < L::kBoxes; ++bx) {
-          tma_load_3d(smem + L::offK + bx * kBoxBytes, tk, bar.kv_full, bx * kBoxCols, un.hkv,
-                      krow);
-          tma_load_3d(smem + L::offV + bx * kBoxBytes, tv, bar.kv_full, bx * kBoxCols, un.hkv,
-                      krow);
+          tma_load_4d(smem + L::offK + bx * kBoxBytes, tk, bar.kv_full, bx * kBoxCols, un.hkv,
+                      kv * kTile, un.b);
+          tma_load_4d(smem + L::offV + bx * kBoxBytes, tv, bar.kv_full, bx * kBoxCols, un.hkv,
+                      kv * kTile, un.b);
         }
       }
       __syncwarp();
@@ -215,15 +215,16 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
           }
           if (elect_one()) {
             mbar_arrive_expect_tx(&bar.full[s], L::kStageBytes + 2 * kTile * 4);
-            const int qrow = un.b * p.S + q * kTile;
             uint8_t *sq = smem + L::offStage + s * L::kStageBytes;
 #pragma unroll
             for (int bx = 0; bx < L::kBoxes; ++bx) {
-              tma_load_3d(sq + bx * kBoxBytes, tq, &bar.full[s], bx * kBoxCols, h, qrow);
-              tma_load_3d(sq + L::kTileBytes + bx * kBoxBytes, tdo, &bar.full[s], bx * kBoxCols,
-                          h, qrow);
+              tma_load_4d(sq + bx * kBoxBytes, tq, &bar.full[s], bx * kBoxCols, h, q * kTile,
+                          un.b);
+              tma_load_4d(sq + L::kTileBytes + bx * kBoxBytes, tdo, &bar.full[s], bx * kBoxCols,
+                          h, q * kTile, un.b);
             }
-            const size_t roff = (size_t)(un.b * p.H + h) * p.S + (size_t)q * kTile;
+            // row vectors are stored per whole tile ([B,H,N*128], zero padding)
+            const size_t roff = ((size_t)(un.b * p.H + h) * p.N + q) * kTile;
             bulk_load(smem + L::offLSE + s * kTile * 4, p.lse2 + roff, kTile * 4, &bar.full[s]);
             bulk_load(smem + L::offDVEC + s * kTile * 4, p.dvec + roff, kTile * 4, &bar.full[s]);
           }
@@ -412,6 +413,9 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
         for (int g = 0; g < p.G; ++g, ++it) {
           const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
           const bool diag = p.causal && (q == kv);
+          // a key row past S (partial last tile) reads zeros; its P is set to zero so that
+          // nothing of it (not even an overflowing exp of -LSE) reaches dS
+          const bool kv_pad = (p.S & (kTile - 1)) != 0 && kv * kTile + r >= p.S;
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
           const uint32_t par = it & 1;
@@ -443,6 +447,10 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
               pk[c / 2] = pack_bf16(pv[0], pv[1]);
               pk[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
             }
+          }
+          if (kv_pad) {  // uniform per thread: outside the exp loop
+#pragma unroll
+            for (int m = 0; m < 32; ++m) pk[m] = 0u;
           }
           // P^T (bf16x2) over the first 32 of this half's S^T columns, all read above: the
           // A operand of G3, which then runs while dS is computed
@@ -709,10 +717,12 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
         }
         uint4 *dkp = reinterpret_cast<uint4 *>(p.dk + orow + ch * 32);
         uint4 *dvp = reinterpret_cast<uint4 *>(p.dv + orow + ch * 32);
+        if (kv * kTile + r < p.S) {  // rows past S belong to no key
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          dkp[j] = make_uint4(kp[4 * j], kp[4 * j + 1], kp[4 * j + 2], kp[4 * j + 3]);
-          dvp[j] = make_uint4(vp[4 * j], vp[4 * j + 1], vp[4 * j + 2], vp[4 * j + 3]);
+          for (int j = 0; j < 4; ++j) {
+            dkp[j] = make_uint4(kp[4 * j], kp[4 * j + 1], kp[4 * j + 2], kp[4 * j + 3]);
+            dvp[j] = make_uint4(vp[4 * j], vp[4 * j + 1], vp[4 * j + 2], vp[4 * j + 3]);
+          }
         }
       }
       ++seg_it;

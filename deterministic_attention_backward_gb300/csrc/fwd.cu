@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     mbar_arrive_expect_tx(bar.q_full, L::kTileBytes);
     for (int bx = 0; bx < L::kBoxes; ++bx)
-      tma_load_3d(smem + L::offQ + bx * kBoxBytes, &tm_q, bar.q_full, bx * kBoxCols, h,
-                  b * p.S + i * kTile);
+      tma_load_4d(smem + L::offQ + bx * kBoxBytes, &tm_q, bar.q_full, bx * kBoxCols, h,
+                  i * kTile, b);
     for (int n = 0; n < T; ++n) {
       const int s = n % L::kStages;
       const uint32_t ph = (n / L::kStages) & 1;
@@ -125,11 +125,11 @@ __global__ void __launch_bounds__(256, 1)
       mbar_arrive_expect_tx(&bar.kv_full[s], pass2 ? 2 * L::kTileBytes : L::kTileBytes);
       uint8_t *sk = smem + L::offStage + s * L::kStageBytes;
       for (int bx = 0; bx < L::kBoxes; ++bx) {
-        tma_load_3d(sk + bx * kBoxBytes, &tm_k, &bar.kv_full[s], bx * kBoxCols, hkv,
-                    b * p.S + j * kTile);
+        tma_load_4d(sk + bx * kBoxBytes, &tm_k, &bar.kv_full[s], bx * kBoxCols, hkv,
+                    j * kTile, b);
         if (pass2)
-          tma_load_3d(sk + L::kTileBytes + bx * kBoxBytes, &tm_v, &bar.kv_full[s],
-                      bx * kBoxCols, hkv, b * p.S + j * kTile);
+          tma_load_4d(sk + L::kTileBytes + bx * kBoxBytes, &tm_v, &bar.kv_full[s],
+                      bx * kBoxCols, hkv, j * kTile, b);
       }
       last[s] = (int)ph;
     }
@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(256, 1)
       const bool pass2 = n >= nkv;
       const int j = pass2 ? n - nkv : n;
       const bool diag = p.causal && (j == i);
+      const int kv_valid = p.S - j * kTile;  // keys of block j inside S (< 128: last tile)
       const uint32_t tsb = tmem + lane_off + L::tS + buf * 128;
       if (!pass2) {
 #pragma unroll 1
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(256, 1)
           float mx = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const bool masked = diag && (ch * 32 + c) > r;
+            const bool masked = (diag && (ch * 32 + c) > r) || (ch * 32 + c) >= kv_valid;
             const float x = masked ? -INFINITY : __uint_as_float(sv[c]) * p.scale_log2;
             sv[c] = __float_as_uint(x);
             mx = fmaxf(mx, x);
@@ -240,8 +241,8 @@ __global__ void __launch_bounds__(256, 1)
           for (int c = 0; c < 32; c += 2) {
             float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2));
             float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), p.scale_log2, -lse2));
-            if (diag && (ch * 32 + c) > r) p0 = 0.f;
-            if (diag && (ch * 32 + c + 1) > r) p1 = 0.f;
+            if ((diag && (ch * 32 + c) > r) || (ch * 32 + c) >= kv_valid) p0 = 0.f;
+            if ((diag && (ch * 32 + c + 1) > r) || (ch * 32 + c + 1) >= kv_valid) p1 = 0.f;
             pk[c / 2] = pack_bf16(p0, p1);
           }
           tmem_st16(tsb + ch * 16, pk);
@@ -254,6 +255,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     if (ok && mbar_wait_warp(bar.o_full, 0, ab)) {
       tc_fence_after();
+      const bool row_ok = i * kTile + r < p.S;  // rows past S (partial last tile): no output
       const size_t orow = ((size_t)(b * p.S + i * kTile + r) * p.H + h) * D;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
@@ -264,11 +266,13 @@ __global__ void __launch_bounds__(256, 1)
         for (int m = 0; m < 16; ++m)
           pk[m] = pack_bf16(__uint_as_float(ov[2 * m]), __uint_as_float(ov[2 * m + 1]));
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow + ch * 32);
+        if (row_ok) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
       }
-      p.lse[(size_t)(b * p.H + h) * p.S + i * kTile + r] = lse2 * kLn2;
+      if (row_ok) p.lse[(size_t)(b * p.H + h) * p.S + i * kTile + r] = lse2 * kLn2;
     }
   }
 

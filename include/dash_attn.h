@@ -19,8 +19,10 @@
  *  - mask: DASH_MASK_FULL, or DASH_MASK_CAUSAL = key j visible to query i iff j <= i
  *    (top-left aligned; queries and keys have the same length S).
  *  - scale <= 0 selects 1/sqrt(D).
- *  - Supported sizes: D in {64, 128}; S a positive multiple of 128; B, H >= 1;
- *    H % group == 0.  Anything else returns DASH_ERR_UNSUPPORTED (or DASH_ERR_INVALID for
+ *  - Supported sizes: D in {64, 128}; S >= 1; B, H >= 1; H % group == 0.  The sequence
+ *    is cut into N = ceil(S/128) tiles; when S is not a multiple of 128 the last tile is
+ *    partial: its rows past S are read as zeros, their keys get zero attention weight, and
+ *    nothing is written for them.  Anything else returns DASH_ERR_UNSUPPORTED (or DASH_ERR_INVALID for
  *    nonsensical values) synchronously and launches nothing.
  *  - Pointers: all tensor and workspace pointers are DEVICE pointers owned by the caller
  *    (for example allocated by PyTorch), 16-byte aligned.  The library allocates no device
@@ -46,7 +48,7 @@ typedef struct CUstream_st *dash_stream_t; /* a cudaStream_t; NULL = legacy defa
 
 typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
 
-/* Tile schedules (gist.science technical summary, section 2.2).  N = S/128 tiles.
+/* Tile schedules (gist.science technical summary, section 2.2).  N = ceil(S/128) tiles.
  *  DASH_SCHED_ATOMIC     -- non-deterministic reference: dQ partials are added with
  *                           unordered atomics (the "non-deterministic counterpart" of
  *                           section 1).  It visits tiles in the SHIFT order (cyclic /
@@ -117,8 +119,9 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
                             dash_stream_t stream);
 
 /* Bytes of device workspace dash_attn_bwd needs: the fp32 dQ accumulator
- * (B*H*S*D*4), two fp32 row vectors (B*H*S*4 each), the dQ ordering semaphores
- * (B*H*(S/128)*4) and a status block; 0 on bad sizes. */
+ * (B*H*Sp*D*4, Sp = 128*ceil(S/128)), two fp32 row vectors (B*H*Sp*4 each), the dQ
+ * ordering semaphores (B*H*(Sp/128)*4) and a status block, each part 256-byte aligned;
+ * 0 on bad sizes. */
 size_t dash_attn_bwd_workspace_bytes(int B, int S, int H, int D);
 
 /* Backward pass (the DASH hot path): given Q, K, V, O, dO and LSE, writes dQ, dK, dV.
@@ -135,8 +138,8 @@ size_t dash_attn_bwd_workspace_bytes(int B, int S, int H, int D);
  *   dq [B,S,H,D]; dk, dv [B,S,H/group,D]                       (outputs, overwritten)
  *   workspace: >= dash_attn_bwd_workspace_bytes(B,S,H,D) bytes, caller-owned, contents
  *   need not be initialised; one workspace must not be used by two calls that may run
- *   concurrently.  Requires S/128 <= number of SMs for DASH_SCHED_SHIFT (all workers of
- *   a head run concurrently); DASH_SCHED_SHIFT with a causal mask requires S/128 even. */
+ *   concurrently.  Requires N <= number of SMs for DASH_SCHED_SHIFT (all workers of
+ *   a head run concurrently); the shift schedules with a causal mask require an even N. */
 dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
                             int B, int S, int H, int group, int D, float scale,
@@ -196,14 +199,14 @@ dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, const void *v,
 const char *dash_status_string(dash_status_t status);
 
 /* Host-only view of the tile schedules the backward kernel executes (no GPU needed).
- * A head has N = S/128 KV blocks and query tiles.  Workers: the per-head units of work
+ * A head has N = ceil(S/128) KV blocks and query tiles.  Workers: the per-head units of work
  * (one KV block, or the pair c, N-1-c for causal DASH_SCHED_SHIFT); each worker runs
  * one or two segments (one KV block each) of steps; step t of a segment visits query
  * tile *q with KV block *kv, and its dQ partial is the rank-th addition into tile q.
  * Return -1 on unsupported arguments. */
 int dash_sched_workers(int sched, int mask, int N);
 /* The schedule dash_attn_bwd runs for `sched` (DASH_SCHED_AUTO resolved, every other value
- * returned unchanged) with `mask` and N = S/128 tiles; -1 on bad arguments. */
+ * returned unchanged) with `mask` and N = ceil(S/128) tiles; -1 on bad arguments. */
 int dash_sched_resolve(int sched, int mask, int N);
 /* Number of CTAs dash_attn_bwd launches for its tile kernel on a GPU with `sms` SMs, for
  * `heads` = B * H/group (batch, kv head) pairs; -1 where dash_attn_bwd would reject the
