@@ -47,6 +47,10 @@ def _load():
             lib.dash_oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, ctypes.c_double, i,
                                             dp, dp, dp, dp, dp]
             lib.dash_oracle_bwd.restype = ctypes.c_int
+            ip = ctypes.POINTER(ctypes.c_int)
+            lib.dash_oracle_bwd_rows.argtypes = [dp, dp, dp, dp, i, i, i, ctypes.c_double, i,
+                                                 i, ip, i, ip, dp, dp, dp]
+            lib.dash_oracle_bwd_rows.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -115,3 +119,33 @@ def attn_bwd_group(q, k, v, do, causal: bool, b: int, g: int, scale: float | Non
     hs = slice(g * G, (g + 1) * G)
     return attn_bwd(q[b:b + 1, :, hs], k[b:b + 1, :, g:g + 1], v[b:b + 1, :, g:g + 1],
                     do[b:b + 1, :, hs], causal, scale)
+
+
+def attn_bwd_rows(q, k, v, do, causal: bool, b: int, g: int, qrows, krows,
+                  scale: float | None = None):
+    """Sampled gradients of one (batch b, kv head g) group at full length: dQ of the query
+    heads g*G .. g*G+G-1 at the query rows ``qrows`` ([len(qrows), G, D]) and dK, dV of kv
+    head g at the key rows ``krows`` ([len(krows), D]), float64 from the same definitions
+    as ``attn_bwd``.  Costs one full row-statistics pass of the group plus O(S*D) per
+    sampled row."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    G = H // Hkv
+    sl = slice(g * G, (g + 1) * G)
+    qs = _f64(q[b, :, sl] if hasattr(q, "detach") else np.asarray(q)[b, :, sl])
+    ds = _f64(do[b, :, sl] if hasattr(do, "detach") else np.asarray(do)[b, :, sl])
+    ks = _f64(k[b, :, g] if hasattr(k, "detach") else np.asarray(k)[b, :, g])
+    vs = _f64(v[b, :, g] if hasattr(v, "detach") else np.asarray(v)[b, :, g])
+    scale = default_scale(D) if scale is None else float(scale)
+    qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int32))
+    kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int32))
+    if qr.size and (qr.min() < 0 or qr.max() >= S) or kr.size and (kr.min() < 0 or kr.max() >= S):
+        raise ValueError("sampled row out of range")
+    dq = np.zeros((qr.size, G, D))
+    dk = np.zeros((kr.size, D))
+    dv = np.zeros((kr.size, D))
+    ip = ctypes.POINTER(ctypes.c_int)
+    _load().dash_oracle_bwd_rows(_ptr(qs), _ptr(ks), _ptr(vs), _ptr(ds), S, G, D, scale,
+                                 int(causal), qr.size, qr.ctypes.data_as(ip), kr.size,
+                                 kr.ctypes.data_as(ip), _ptr(dq), _ptr(dk), _ptr(dv))
+    return dq, dk, dv

@@ -181,3 +181,107 @@ int dash_oracle_bwd(const double *q, const double *k, const double *v, const dou
   free(Dvec);
   return threads;
 }
+
+/* Sampled gradients of one (batch, kv head) group at full length, for parity checks at
+ * sizes where the whole backward is too slow on the CPU.  Same definitions as above,
+ * evaluated for chosen rows only: LSE_i and Dvec_i for every query row of every head of
+ * the group (a full pass), then dQ_i (each query head) for the query rows qrows[0..nq)
+ * and dK_j, dV_j (summed over the group's heads) for the key rows krows[0..nk).
+ * Slice layout: q, dout [S, G, D]; k, v [S, D]; dq out [nq, G, D]; dk, dv out [nk, D].
+ * Returns the number of OpenMP threads used. */
+#define SQ(i, hh, d) (((size_t)(i) * G + (hh)) * D + (d))
+#define SK(j, d) ((size_t)(j) * D + (d))
+int dash_oracle_bwd_rows(const double *q, const double *k, const double *v,
+                         const double *dout, int S, int G, int D, double scale, int causal,
+                         int nq, const int *qrows, int nk, const int *krows, double *dq,
+                         double *dk, double *dv) {
+  if (S <= 0 || G <= 0 || D <= 0 || nq < 0 || nk < 0) return 0;
+  double *LSE = (double *)malloc(sizeof(double) * (size_t)G * S);
+  double *Dvec = (double *)malloc(sizeof(double) * (size_t)G * S);
+  int threads = 1;
+#pragma omp parallel
+  {
+#ifdef _OPENMP
+#pragma omp single
+    threads = omp_get_num_threads();
+#endif
+    double *s = (double *)malloc(sizeof(double) * (size_t)S);
+    double *orow = (double *)malloc(sizeof(double) * (size_t)D);
+    /* LSE_i, O_i and Dvec_i of every row of every head of the group */
+#pragma omp for schedule(dynamic, 4)
+    for (long long r = 0; r < (long long)G * S; ++r) {
+      const int hh = (int)(r / S), i = (int)(r % S);
+      double m = -INFINITY;
+      for (int j = 0; j < S; ++j) {
+        if (!allowed(causal, i, j)) continue;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += q[SQ(i, hh, d)] * k[SK(j, d)];
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+      }
+      double l = 0.0;
+      for (int j = 0; j < S; ++j)
+        if (allowed(causal, i, j)) l += exp(s[j] - m);
+      const double L = m + log(l);
+      for (int d = 0; d < D; ++d) orow[d] = 0.0;
+      for (int j = 0; j < S; ++j) {
+        if (!allowed(causal, i, j)) continue;
+        const double p = exp(s[j] - L);
+        for (int d = 0; d < D; ++d) orow[d] += p * v[SK(j, d)];
+      }
+      double dvec = 0.0;
+      for (int d = 0; d < D; ++d) dvec += dout[SQ(i, hh, d)] * orow[d];
+      LSE[(size_t)hh * S + i] = L;
+      Dvec[(size_t)hh * S + i] = dvec;
+    }
+    /* dQ_i = scale sum_j P_ij (dP_ij - Dvec_i) K_j for the sampled query rows */
+#pragma omp for schedule(dynamic, 1)
+    for (long long r = 0; r < (long long)nq * G; ++r) {
+      const int n = (int)(r / G), hh = (int)(r % G), i = qrows[n];
+      for (int d = 0; d < D; ++d) dq[((size_t)n * G + hh) * D + d] = 0.0;
+      for (int j = 0; j < S; ++j) {
+        if (!allowed(causal, i, j)) continue;
+        double sc = 0.0, dp = 0.0;
+        for (int d = 0; d < D; ++d) {
+          sc += q[SQ(i, hh, d)] * k[SK(j, d)];
+          dp += dout[SQ(i, hh, d)] * v[SK(j, d)];
+        }
+        const double p = exp(scale * sc - LSE[(size_t)hh * S + i]);
+        const double ds = p * (dp - Dvec[(size_t)hh * S + i]);
+        for (int d = 0; d < D; ++d) dq[((size_t)n * G + hh) * D + d] += scale * ds * k[SK(j, d)];
+      }
+    }
+    /* dV_j = sum_hh sum_i P_ij dO_i and dK_j = scale sum_hh sum_i dS_ij Q_i, sampled key rows */
+#pragma omp for schedule(dynamic, 1)
+    for (int n = 0; n < nk; ++n) {
+      const int j = krows[n];
+      for (int d = 0; d < D; ++d) {
+        dk[(size_t)n * D + d] = 0.0;
+        dv[(size_t)n * D + d] = 0.0;
+      }
+      for (int hh = 0; hh < G; ++hh) {
+        for (int i = 0; i < S; ++i) {
+          if (!allowed(causal, i, j)) continue;
+          double sc = 0.0, dp = 0.0;
+          for (int d = 0; d < D; ++d) {
+            sc += q[SQ(i, hh, d)] * k[SK(j, d)];
+            dp += dout[SQ(i, hh, d)] * v[SK(j, d)];
+          }
+          const double p = exp(scale * sc - LSE[(size_t)hh * S + i]);
+          const double ds = p * (dp - Dvec[(size_t)hh * S + i]);
+          for (int d = 0; d < D; ++d) {
+            dv[(size_t)n * D + d] += p * dout[SQ(i, hh, d)];
+            dk[(size_t)n * D + d] += scale * ds * q[SQ(i, hh, d)];
+          }
+        }
+      }
+    }
+    free(s);
+    free(orow);
+  }
+  free(LSE);
+  free(Dvec);
+  return threads;
+}
+#undef SQ
+#undef SK

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle
+from dash_inputs import make_qkv_do
 
 CASES = [  # (B, S, H, Hkv, D)
     (1, 1, 2, 2, 3),
@@ -219,3 +220,23 @@ def test_group_slice_equals_whole():
     gq, gk, gv, _, _ = oracle.attn_bwd_group(q, k, v, do, True, b=1, g=1)
     assert np.array_equal(gq[0], dq[1, :, 2:4]) and np.array_equal(gk[0], dk[1, :, 1:2])
     assert np.array_equal(gv[0], dv[1, :, 1:2])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,S,H,Hkv,D", [(2, 37, 4, 2, 16), (1, 64, 2, 2, 8), (1, 50, 4, 1, 12)])
+def test_sampled_rows_equal_the_full_backward(B, S, H, Hkv, D, causal):
+    """The sampled-row oracle (used for parity at full sizes) restates the same definitions
+    row by row: its rows equal the full backward's rows to rounding."""
+    q, k, v, do = make_qkv_do(B, S, H, Hkv, D, seed=11)
+    dq, dk, dv, _, _ = oracle.attn_bwd(q, k, v, do, causal)
+    G = H // Hkv
+    rng = np.random.default_rng(0)
+    for b in range(B):
+        for g in range(Hkv):
+            qr = sorted(set([0, S - 1] + list(rng.integers(0, S, 5))))
+            kr = sorted(set([0, S - 1] + list(rng.integers(0, S, 5))))
+            sq, sk, sv = oracle.attn_bwd_rows(q, k, v, do, causal, b, g, qr, kr)
+            ref_q = dq[b, qr][:, g * G:(g + 1) * G]
+            np.testing.assert_allclose(sq, ref_q, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(sk, dk[b, kr, g], rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(sv, dv[b, kr, g], rtol=1e-10, atol=1e-12)
