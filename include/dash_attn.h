@@ -98,7 +98,7 @@ typedef enum {
 typedef enum {
   DASH_OK = 0,
   DASH_ERR_INVALID = 1,     /* null pointer, non-positive size, misaligned pointer    */
-  DASH_ERR_UNSUPPORTED = 2, /* valid but outside this build's support (D, S, N, GPU)  */
+  DASH_ERR_UNSUPPORTED = 2, /* valid but outside this library's support (D, N, GPU)  */
   DASH_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed            */
   DASH_ERR_TIMEOUT = 4,     /* a device-side bounded wait ran out (status word set)   */
   DASH_ERR_WORKSPACE = 5    /* workspace NULL or smaller than required                */
