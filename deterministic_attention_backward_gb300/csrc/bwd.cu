@@ -6,7 +6,7 @@
 // operations run back to back on one SM with on-chip accumulation) and visits query
 // tiles in the order of the selected schedule (section 2.2).  Per visited tile (128 query
 // rows i, all in one query head h) it runs the five dense contractions on the tcgen05
-// tensor cores, G3 and G4 split into the two 64-column halves a/b of the query tile:
+// tensor cores, G4 split into the two 64-column halves a/b of the query tile:
 //   G1  S^T  = K_j Q_i^T                   (128 x 128 x D)  -> TMEM
 //   G2  dP^T = V_j dO_i^T                  (128 x 128 x D)  -> TMEM
 //       P^T  = exp2(S^T * scale*log2e - LSE_i*log2e)   [causal: 0 above the diagonal]
@@ -245,15 +245,15 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
 
 // ---------------------------------------------------------------------------------------
 // MMA issuer: the whole warp runs the loop (waits, descriptors and control flow stay
-// warp-uniform); one elected lane issues each tcgen05 instruction.  Within a segment the
-// S^T product of the next step is issued as soon as the softmax-gradient warps have read
-// the current S^T, so it runs while they compute P and dS.
+// warp-uniform); one elected lane issues each tcgen05 instruction.  Once the
+// softmax-gradient warps have written P^T over the current S^T columns, G3 and then the
+// next step's S^T product are issued, so both run while those warps compute dS.
 template <int D, bool DET>
 __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
                         const Abort &ab) {
   using L = BwdLayout<D, DET>;
   constexpr uint32_t kIdescSS = make_idesc_bf16(128, 128, false, false);  // G1, G2
-  constexpr uint32_t kIdescTS = make_idesc_bf16(128, D, false, true);     // G3x, G4x
+  constexpr uint32_t kIdescTS = make_idesc_bf16(128, D, false, true);     // G3, G4x
   constexpr uint32_t kIdescG5 = make_idesc_bf16(128, D, true, true);      // G5
   const uint32_t sbase = smem_u32(smem);
   // K-major views (contraction over D): k step of 16 columns = +32 B inside a box, boxes
@@ -824,11 +824,6 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 }
 
 }  // namespace
-
-size_t bwd_smem_bytes(int D, bool deterministic) {
-  if (D == 64) return deterministic ? BwdLayout<64, true>::kBytes : BwdLayout<64, false>::kBytes;
-  return deterministic ? BwdLayout<128, true>::kBytes : BwdLayout<128, false>::kBytes;
-}
 
 cudaError_t launch_bwd(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, int grid,

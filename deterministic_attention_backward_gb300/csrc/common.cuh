@@ -67,7 +67,6 @@ struct FwdParams {
   float scale_log2;
 };
 
-size_t bwd_smem_bytes(int D, bool deterministic);
 size_t fwd_smem_bytes(int D);
 
 cudaError_t launch_bwd(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -39,8 +39,8 @@
 
 namespace dash {
 
-// kShiftFill is the shift schedule on as many SMs as hold whole heads, plus DESCENDING on
-// the remaining SMs for a share of the heads (the host decides the split).
+// kShiftFill is the packed shift schedule (below): the shift workers of all heads dealt to
+// every CTA of the grid; on the device it runs the kShift traversal with packed ranks.
 enum Sched : int { kAtomic = 0, kSerial = 1, kDescending = 2, kShift = 3, kShiftFill = 4 };
 
 // Which visiting order a schedule uses (ATOMIC borrows the shift order when it exists; the
