@@ -19,7 +19,8 @@ import os
 import threading
 
 __all__ = ["fwd", "bwd", "bwd_workspace_bytes", "fwd_workspace_bytes", "status",
-           "sched_table", "sched_grid", "sched_resolve", "packed_rank", "SCHEDULES", "lib", "DashError"]
+           "sched_table", "sched_grid", "sched_resolve", "packed_rank", "fwd_varlen",
+           "bwd_varlen", "SCHEDULES", "lib", "DashError"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdash_attn.so")
@@ -31,7 +32,8 @@ EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_work
            "dash_attn_bwd", "dash_attn_bwd_stages", "dash_attn_status",
            "dash_status_string", "dash_sched_workers", "dash_sched_segments", "dash_sched_steps",
            "dash_sched_step", "dash_sched_grid", "dash_sched_packed_rank", "dash_sched_resolve",
-           "dash_attn_bwd_noalloc"]
+           "dash_attn_bwd_noalloc", "dash_attn_bwd_varlen_workspace_bytes",
+           "dash_attn_fwd_varlen", "dash_attn_bwd_varlen"]
 
 
 class DashError(RuntimeError):
@@ -71,6 +73,13 @@ def lib() -> ctypes.CDLL:
         L.dash_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                             f, i, i, vp]
         L.dash_attn_bwd_noalloc.restype = i
+        L.dash_attn_bwd_varlen_workspace_bytes.argtypes = [ip, i, i, i]
+        L.dash_attn_bwd_varlen_workspace_bytes.restype = sz
+        L.dash_attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, ip, i, i, i, i, f, i, vp, sz, vp]
+        L.dash_attn_fwd_varlen.restype = i
+        L.dash_attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, i, i, i, i, f,
+                                           i, i, vp, sz, vp]
+        L.dash_attn_bwd_varlen.restype = i
         L.dash_attn_status.argtypes = [vp, vp]
         L.dash_attn_status.restype = i
         L.dash_status_string.argtypes = [i]
@@ -246,3 +255,66 @@ def sched_table(schedule: str, causal: bool, N: int):
             segs.append(steps)
         out.append(segs)
     return out
+
+
+def _cu(cu_seqlens):
+    import numpy as np
+    cu = np.ascontiguousarray(np.asarray(
+        cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int32))
+    if cu.ndim != 1 or cu.size < 2:
+        raise ValueError("cu_seqlens must hold batch+1 offsets")
+    return cu, cu.size - 1, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+
+
+def fwd_varlen(q, k, v, cu_seqlens, causal: bool = False, scale: float | None = None,
+               stream=None, check: bool = False):
+    """Forward over a packed batch: q [T,H,D], k/v [T,Hkv,D], ``cu_seqlens`` (host) the
+    batch+1 token offsets.  Returns O [T,H,D] and LSE (the sequences' [H,S_b] blocks one
+    after another, flat fp32 of T*H values)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, torch.bfloat16)
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    cu, batch, cp = _cu(cu_seqlens)
+    if int(cu[-1]) != T:
+        raise ValueError("cu_seqlens[-1] must equal the number of tokens")
+    o = torch.empty_like(q)
+    lse = torch.empty(T * H, dtype=torch.float32, device=q.device)
+    ws = _workspace(256, q.device)
+    code = lib().dash_attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), cp, batch, H, H // Hkv, D,
+                                      float(scale) if scale else 0.0, int(bool(causal)),
+                                      ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    _check(code, "dash_attn_fwd_varlen")
+    if check:
+        status(ws, stream)
+    return o, lse
+
+
+def bwd_varlen(q, k, v, o, do, lse, cu_seqlens, causal: bool = False, schedule: str = "auto",
+               scale: float | None = None, stream=None, check: bool = False):
+    """Backward over a packed batch (layouts as ``fwd_varlen``): returns dQ, dK, dV."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _require(t, n, torch.bfloat16)
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    cu, batch, cp = _cu(cu_seqlens)
+    if int(cu[-1]) != T:
+        raise ValueError("cu_seqlens[-1] must equal the number of tokens")
+    if schedule not in SCHEDULES:
+        raise ValueError(f"schedule must be one of {sorted(SCHEDULES)}")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = lib().dash_attn_bwd_varlen_workspace_bytes(cp, batch, H, D)
+    ws = _workspace(max(int(nbytes), 256), q.device)
+    code = lib().dash_attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                      dv.data_ptr(), cp, batch, H, H // Hkv, D,
+                                      float(scale) if scale else 0.0, int(bool(causal)),
+                                      SCHEDULES[schedule], ws.data_ptr(), ws.numel(),
+                                      _stream_ptr(stream))
+    _check(code, "dash_attn_bwd_varlen")
+    if check:
+        status(ws, stream)
+    return dq, dk, dv

@@ -73,6 +73,7 @@ dash_status_t device_info(DevInfo *out) {
 
 // ------------------------------------------------------------------ validation / workspace
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 int tiles(int S) { return (S + kTile - 1) / kTile; }  // N: a last, partial tile counts
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -164,15 +165,17 @@ size_t dash_attn_bwd_workspace_bytes(int B, int S, int H, int D) {
   return carve_bwd(nullptr, B, S, H, D).total;
 }
 
-dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
-                            int B, int S, int H, int group, int D, float scale,
-                            dash_mask_t mask, void *workspace, size_t workspace_bytes,
-                            dash_stream_t stream) {
+// keep_status: leave the workspace status word as it is (a later sequence of a varlen
+// batch adds its error flags to the earlier ones' instead of clearing them).
+static dash_status_t fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int S, int H, int group, int D, float scale,
+                              dash_mask_t mask, void *workspace, size_t workspace_bytes,
+                              dash_stream_t stream, bool keep_status) {
   dash_status_t st = check_sizes(B, S, H, group, D);
   if (st != DASH_OK) return st;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
   if (!q || !k || !v || !o || !lse) return DASH_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
     return DASH_ERR_INVALID;
   if (!workspace || workspace_bytes < kStatusBytes || !aligned16(workspace))
     return DASH_ERR_WORKSPACE;
@@ -184,7 +187,8 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
       !make_bshd_map(&tv, v, B, S, Hkv, D))
     return DASH_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return DASH_ERR_CUDA;
+  if (!keep_status && cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess)
+    return DASH_ERR_CUDA;
   dash::FwdParams p{};
   p.o = static_cast<__nv_bfloat16 *>(o);
   p.lse = lse;
@@ -200,21 +204,30 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
   return dash::launch_fwd(D, tq, tk, tv, p, s) == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
-dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, const void *o,
-                                   const void *dout, const float *lse, void *dq, void *dk,
-                                   void *dv, int B, int S, int H, int group, int D, float scale,
-                                   dash_mask_t mask, dash_sched_t sched, void *workspace,
-                                   size_t workspace_bytes, unsigned stages,
-                                   dash_stream_t stream) {
+dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int S, int H, int group, int D, float scale,
+                            dash_mask_t mask, void *workspace, size_t workspace_bytes,
+                            dash_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, S, H, group, D, scale, mask, workspace, workspace_bytes,
+                  stream, false);
+}
+
+static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *o,
+                              const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                              int B, int S, int H, int group, int D, float scale,
+                              dash_mask_t mask, dash_sched_t sched, void *workspace,
+                              size_t workspace_bytes, unsigned stages, dash_stream_t stream,
+                              bool keep_status) {
   if (stages == 0 || (stages & ~unsigned(DASH_BWD_ALL))) return DASH_ERR_INVALID;
   dash_status_t st = check_sizes(B, S, H, group, D);
   if (st != DASH_OK) return st;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
   if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_AUTO) return DASH_ERR_INVALID;
   sched = (dash_sched_t)resolve_sched(sched, mask, tiles(S));
-  const void *ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
+  const void *ptrs[] = {q, k, v, o, dout, dq, dk, dv};
   for (const void *ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return DASH_ERR_INVALID;
+  if (!lse || !aligned4(lse)) return DASH_ERR_INVALID;
   const int N = tiles(S);
   const int causal = mask == DASH_MASK_CAUSAL;
   const bool shift = sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL;
@@ -239,7 +252,9 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   const float sc = resolve_scale(scale, D);
   if (stages & DASH_BWD_PROLOGUE) {
     // status word + dQ accumulator are contiguous; semaphores separately
-    if (cudaMemsetAsync(w.status, 0, kStatusBytes + w.dqacc_bytes, s) != cudaSuccess ||
+    if ((keep_status ? cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes, s)
+                     : cudaMemsetAsync(w.status, 0, kStatusBytes + w.dqacc_bytes, s)) !=
+            cudaSuccess ||
         cudaMemsetAsync(w.sem, 0, w.sem_bytes, s) != cudaSuccess)
       return DASH_ERR_CUDA;
     // a partial last tile: its padding rows of lse2 / Dvec must read as zero
@@ -292,6 +307,16 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
   return DASH_OK;
 }
 
+dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse, void *dq, void *dk,
+                                   void *dv, int B, int S, int H, int group, int D, float scale,
+                                   dash_mask_t mask, dash_sched_t sched, void *workspace,
+                                   size_t workspace_bytes, unsigned stages,
+                                   dash_stream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, S, H, group, D, scale, mask, sched,
+                  workspace, workspace_bytes, stages, stream, false);
+}
+
 dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
                             int B, int S, int H, int group, int D, float scale,
@@ -299,6 +324,98 @@ dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const v
                             size_t workspace_bytes, dash_stream_t stream) {
   return dash_attn_bwd_stages(q, k, v, o, dout, lse, dq, dk, dv, B, S, H, group, D, scale, mask,
                               sched, workspace, workspace_bytes, DASH_BWD_ALL, stream);
+}
+
+// ------------------------------------------------------------------ variable-length batches
+// The sequences of a packed batch are independent attention problems: each runs as the
+// B = 1 problem on its own slices, one after another on `stream`, sharing the workspace.
+static dash_status_t check_seqlens(const int *cu, int batch, int *max_len) {
+  if (!cu || batch <= 0 || cu[0] != 0) return DASH_ERR_INVALID;
+  int mx = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (cu[b + 1] < cu[b]) return DASH_ERR_INVALID;
+    mx = cu[b + 1] - cu[b] > mx ? cu[b + 1] - cu[b] : mx;
+  }
+  *max_len = mx;
+  return DASH_OK;
+}
+
+size_t dash_attn_bwd_varlen_workspace_bytes(const int *cu_seqlens, int batch, int H, int D) {
+  int mx = 0;
+  if (check_seqlens(cu_seqlens, batch, &mx) != DASH_OK || mx == 0) return 0;
+  return dash_attn_bwd_workspace_bytes(1, mx, H, D);
+}
+
+dash_status_t dash_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, const int *cu_seqlens, int batch, int H,
+                                   int group, int D, float scale, dash_mask_t mask,
+                                   void *workspace, size_t workspace_bytes,
+                                   dash_stream_t stream) {
+  int mx = 0;
+  dash_status_t st = check_seqlens(cu_seqlens, batch, &mx);
+  if (st != DASH_OK) return st;
+  if (H <= 0 || group <= 0 || H % group) return DASH_ERR_INVALID;
+  const int Hkv = H / group;
+  bool first = true;
+  for (int b = 0; b < batch; ++b) {
+    const int s0 = cu_seqlens[b], S = cu_seqlens[b + 1] - s0;
+    if (S == 0) continue;
+    st = fwd_impl(static_cast<const __nv_bfloat16 *>(q) + (size_t)s0 * H * D,
+                  static_cast<const __nv_bfloat16 *>(k) + (size_t)s0 * Hkv * D,
+                  static_cast<const __nv_bfloat16 *>(v) + (size_t)s0 * Hkv * D,
+                  static_cast<__nv_bfloat16 *>(o) + (size_t)s0 * H * D, lse + (size_t)s0 * H, 1,
+                  S, H, group, D, scale, mask, workspace, workspace_bytes, stream, !first);
+    if (st != DASH_OK) return st;
+    first = false;
+  }
+  return DASH_OK;
+}
+
+dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse, void *dq, void *dk,
+                                   void *dv, const int *cu_seqlens, int batch, int H, int group,
+                                   int D, float scale, dash_mask_t mask, dash_sched_t sched,
+                                   void *workspace, size_t workspace_bytes,
+                                   dash_stream_t stream) {
+  int mx = 0;
+  dash_status_t st = check_seqlens(cu_seqlens, batch, &mx);
+  if (st != DASH_OK) return st;
+  if (H <= 0 || group <= 0 || H % group) return DASH_ERR_INVALID;
+  if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
+  if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_AUTO) return DASH_ERR_INVALID;
+  // refuse before enqueuing anything: every sequence must be runnable with this schedule
+  DevInfo dev;
+  if ((st = device_info(&dev)) != DASH_OK) return st;
+  const int Hkv = H / group;
+  for (int b = 0; b < batch; ++b) {
+    const int S = cu_seqlens[b + 1] - cu_seqlens[b];
+    if (S == 0) continue;
+    if ((st = check_sizes(1, S, H, group, D)) != DASH_OK) return st;
+    const int N = tiles(S), rs = resolve_sched(sched, mask, N);
+    LaunchPlan plan;
+    if (((rs == DASH_SCHED_SHIFT || rs == DASH_SCHED_SHIFT_FILL) && mask == DASH_MASK_CAUSAL &&
+         (N % 2)) ||
+        !make_plan(rs, mask == DASH_MASK_CAUSAL, N, Hkv, dev.sms, &plan))
+      return DASH_ERR_UNSUPPORTED;
+  }
+  if (workspace_bytes < dash_attn_bwd_workspace_bytes(1, mx, H, D)) return DASH_ERR_WORKSPACE;
+  bool first = true;
+  for (int b = 0; b < batch; ++b) {
+    const int s0 = cu_seqlens[b], S = cu_seqlens[b + 1] - s0;
+    if (S == 0) continue;
+    const size_t qo = (size_t)s0 * H * D, ko = (size_t)s0 * Hkv * D;
+    st = bwd_impl(static_cast<const __nv_bfloat16 *>(q) + qo,
+                  static_cast<const __nv_bfloat16 *>(k) + ko,
+                  static_cast<const __nv_bfloat16 *>(v) + ko,
+                  static_cast<const __nv_bfloat16 *>(o) + qo,
+                  static_cast<const __nv_bfloat16 *>(dout) + qo, lse + (size_t)s0 * H,
+                  static_cast<__nv_bfloat16 *>(dq) + qo, static_cast<__nv_bfloat16 *>(dk) + ko,
+                  static_cast<__nv_bfloat16 *>(dv) + ko, 1, S, H, group, D, scale, mask, sched,
+                  workspace, workspace_bytes, DASH_BWD_ALL, stream, !first);
+    if (st != DASH_OK) return st;
+    first = false;
+  }
+  return DASH_OK;
 }
 
 dash_status_t dash_attn_status(void *workspace, dash_stream_t stream) {

@@ -25,7 +25,7 @@
  *    nothing is written for them.  Anything else returns DASH_ERR_UNSUPPORTED (or DASH_ERR_INVALID for
  *    nonsensical values) synchronously and launches nothing.
  *  - Pointers: all tensor and workspace pointers are DEVICE pointers owned by the caller
- *    (for example allocated by PyTorch), 16-byte aligned.  The library allocates no device
+ *    (for example allocated by PyTorch), 16-byte aligned (LSE: 4-byte aligned).  The library allocates no device
  *    memory, keeps no state between calls other than per-device kernel attributes, and is
  *    safe to call from several host threads on different streams.
  *  - Asynchrony: calls enqueue work on `stream` and return; argument errors are reported
@@ -194,6 +194,32 @@ dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, const void *v,
                                     const void *dout, const float *lse, void *dq, void *dk,
                                     void *dv, int B, int S, int H, int group, int D, float scale,
                                     dash_mask_t mask, dash_sched_t sched, dash_stream_t stream);
+
+/* Variable-length batches.  `batch` sequences packed along the token axis:
+ *   Q, O, dO, dQ : [T, H, D]        K, V, dK, dV : [T, Hkv, D]      T = cu_seqlens[batch]
+ *   LSE          : the sequences' [H, S_b] blocks one after another (sequence b's block
+ *                  starts at float offset H * cu_seqlens[b]); 4-byte aligned
+ *   cu_seqlens   : HOST array of batch+1 ints, cu_seqlens[0] = 0, non-decreasing; sequence
+ *                  b is tokens [cu_seqlens[b], cu_seqlens[b+1]) (S_b may be 0 or any length).
+ * Each sequence is an independent attention problem (the mask applies within it) and runs
+ * as the B = 1 call on its slices, one after another on `stream`, so its results -- and
+ * their bit-identity under an ordered schedule -- are those of that call.  The workspace is
+ * shared by the sequences: size it with dash_attn_bwd_varlen_workspace_bytes (the longest
+ * sequence's need).  The backward checks every sequence against the schedule before it
+ * enqueues anything (DASH_SCHED_AUTO picks per sequence); the device status word collects
+ * the flags of all sequences.  Returns as the B = 1 calls do. */
+size_t dash_attn_bwd_varlen_workspace_bytes(const int *cu_seqlens, int batch, int H, int D);
+dash_status_t dash_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, const int *cu_seqlens, int batch, int H,
+                                   int group, int D, float scale, dash_mask_t mask,
+                                   void *workspace, size_t workspace_bytes,
+                                   dash_stream_t stream);
+dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse, void *dq, void *dk,
+                                   void *dv, const int *cu_seqlens, int batch, int H, int group,
+                                   int D, float scale, dash_mask_t mask, dash_sched_t sched,
+                                   void *workspace, size_t workspace_bytes,
+                                   dash_stream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *dash_status_string(dash_status_t status);

@@ -142,3 +142,23 @@ def test_auto_schedule_resolution(L, causal, N):
     assert dash.sched_table("auto", causal, N) == dash.sched_table(want, causal, N)
     assert dash.sched_grid("auto", causal, N, 64, 152) == dash.sched_grid(want, causal, N, 64, 152)
     assert L.dash_sched_resolve(6, int(causal), N) == -1
+
+
+def test_varlen_arguments_and_workspace(L):
+    """Packed-batch entry points: offsets are checked before anything runs, and the shared
+    workspace is the longest sequence's need."""
+    import ctypes as ct
+    arr = lambda xs: (ct.c_int * len(xs))(*xs)
+    fake = 1 << 20
+    cu = arr([0, 200, 712, 749])
+    assert L.dash_attn_bwd_varlen_workspace_bytes(cu, 3, 4, 64) == \
+        dash.bwd_workspace_bytes(1, 512, 4, 64)
+    assert L.dash_attn_bwd_varlen_workspace_bytes(arr([0, 5, 3]), 2, 4, 64) == 0   # decreasing
+    assert L.dash_attn_bwd_varlen_workspace_bytes(arr([1, 5]), 1, 4, 64) == 0      # cu[0] != 0
+    args = [fake] * 9
+    assert L.dash_attn_bwd_varlen(*args, arr([0, 5, 3]), 2, 4, 1, 64, 0.0, 0, 1, fake, 1 << 30,
+                                  None) == 1
+    assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 3, 64, 0.0, 0, 1, fake, 1 << 30, None) == 1
+    assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 1, 64, 0.0, 0, 9, fake, 1 << 30, None) == 1
+    assert L.dash_attn_fwd_varlen(*([fake] * 5), arr([2, 4]), 1, 4, 1, 64, 0.0, 0, fake, 256,
+                                  None) == 1
