@@ -288,23 +288,48 @@ def run_gpu(args, wl, rank, world):
             h2d += sum(t.numel() * t.element_size() for t in hs.values())
             d2h += sum(t.numel() * t.element_size() for t in outs.values())
 
+        # three streams, so that the copies of one sweep point overlap the backward of the
+        # previous one: inputs in, compute (the current stream), results out; a point's
+        # buffers are refilled only after its previous backward and read-out are done
+        comp = torch.cuda.current_stream()
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        done = [None] * len(probs)   # backward of point j finished (its inputs are free)
+        out_done = [None] * len(probs)  # read-out of point j finished (its outputs are free)
+
         def e2e_step():
-            for p, (hs, outs) in zip(probs, host):
-                for n, t in hs.items():
-                    p[n].copy_(t, non_blocking=True)
+            for j, (p, (hs, outs)) in enumerate(zip(probs, host)):
+                with torch.cuda.stream(s_in):
+                    if done[j] is not None:
+                        s_in.wait_event(done[j])
+                    for n, t in hs.items():
+                        p[n].copy_(t, non_blocking=True)
+                    ev_in = torch.cuda.Event()
+                    ev_in.record(s_in)
+                comp.wait_event(ev_in)
+                if out_done[j] is not None:
+                    comp.wait_event(out_done[j])
                 call(p, sched)
-                for n, t in outs.items():
-                    t.copy_(p[n], non_blocking=True)
+                done[j] = torch.cuda.Event()
+                done[j].record(comp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done[j])
+                    for n, t in outs.items():
+                        t.copy_(p[n], non_blocking=True)
+                    out_done[j] = torch.cuda.Event()
+                    out_done[j].record(s_out)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n_e2e = max(1, min(args.steps, 5))
-        a.record()
+        a.record(comp)
+        s_in.wait_event(a)
         for _ in range(n_e2e):
             e2e_step()
-        b.record()
+        for ev in out_done:
+            comp.wait_event(ev)
+        b.record(comp)
         torch.cuda.synchronize()
         e2e_val = step_flops * n_e2e / (a.elapsed_time(b) / 1e3) / 1e12 * world
 
