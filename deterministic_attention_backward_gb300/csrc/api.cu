@@ -136,15 +136,16 @@ int resolve_sched(int sched, int mask, int N) {
   return (mask == DASH_MASK_CAUSAL && (N % 2)) ? DASH_SCHED_DESCENDING : DASH_SCHED_SHIFT_FILL;
 }
 
-// False when a shift schedule cannot have every worker of a head resident at once.
+// False when plain SHIFT cannot have every worker of a head resident at once.  SHIFT_FILL
+// has no such limit: its ranks follow the time order of the rounds, so a head wider than
+// the grid simply spans more rounds.
 bool make_plan(int sched, int causal, int N, int heads, int sms, LaunchPlan *pl) {
   pl->sched = dash::traversal(sched, causal, N);
   pl->workers = dash::sched_workers(pl->sched, causal, N);
   const long long total = (long long)heads * pl->workers;
   pl->grid = (int)(total < sms ? total : sms);
   pl->packed = sched == DASH_SCHED_SHIFT_FILL;
-  const bool shift = sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL;
-  return !(shift && pl->workers > sms);
+  return !(sched == DASH_SCHED_SHIFT && pl->workers > sms);
 }
 
 float resolve_scale(float scale, int D) {
@@ -486,7 +487,7 @@ int dash_sched_packed_rank(int mask, int N, int heads, int grid, int head, int q
       head >= heads || q < 0 || q >= N || kv < 0 || kv >= N || (mask && kv > q))
     return -1;
   const int W = dash::sched_workers(dash::kShift, mask, N);
-  if (grid < W || grid > heads * W) return -1;
+  if (grid < 1 || grid > heads * W) return -1;
   return dash::packed_rank(mask, N, grid, head, q, kv);
 }
 

@@ -75,8 +75,10 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           the earlier phase's partials first, then the later phase's, each
  *                           phase in its shift (step) order.  Heads inside one round get
  *                           exactly the DASH_SCHED_SHIFT order.  Keeps every SM busy where
- *                           plain SHIFT leaves SMs waiting for a head's remaining workers.
- *                           Deterministic for a given SM count (dash_sched_grid,
+ *                           plain SHIFT leaves SMs waiting for a head's remaining workers,
+ *                           and has no limit on N: a head with more workers than SMs runs
+ *                           as several phases, each dQ tile adding the earlier phases'
+ *                           partials first.  Deterministic for a given SM count (dash_sched_grid,
  *                           dash_sched_packed_rank give the order).
  *  DASH_SCHED_AUTO       -- the deterministic schedule that measured fastest on GB300 for
  *                           the mask and tile count (dash_sched_resolve names it): the pages
@@ -236,7 +238,7 @@ int dash_sched_workers(int sched, int mask, int N);
 int dash_sched_resolve(int sched, int mask, int N);
 /* Number of CTAs dash_attn_bwd launches for its tile kernel on a GPU with `sms` SMs, for
  * `heads` = B * H/group (batch, kv head) pairs; -1 where dash_attn_bwd would reject the
- * schedule arguments (e.g. a shift schedule whose workers per head exceed the SMs). */
+ * schedule arguments (e.g. DASH_SCHED_SHIFT with more workers per head than SMs). */
 int dash_sched_grid(int sched, int mask, int N, int heads, int sms);
 /* DASH_SCHED_SHIFT_FILL: position of KV block kv's partial in dQ tile q of head `head`
  * (0 <= head < heads) when the tile kernel runs on `grid` CTAs (dash_sched_grid); -1 on

@@ -98,10 +98,11 @@ def test_atomic_odd_causal_falls_back_to_serial_traversal(L):
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N,heads,P", [(8, 5, 12), (8, 3, 8), (16, 4, 24), (4, 9, 10), (32, 3, 38),
-                                       (32, 64, 152), (64, 8, 152), (16, 20, 152)])
+                                       (32, 64, 152), (64, 8, 152), (16, 20, 152),
+                                       (16, 3, 5), (32, 2, 10), (64, 1, 31), (24, 2, 7)])
 def test_packed_ranks_equal_oracle(L, causal, N, heads, P):
     """The library's packed-shift ranks equal the oracle's lock-step simulation of the
-    workers dealt round-robin to P CTAs."""
+    workers dealt round-robin to P CTAs, also when a head has more workers than CTAs."""
     W = N // 2 if causal else N
     if P > heads * W:
         P = heads * W
@@ -122,6 +123,9 @@ def test_grid_sizes(L, causal):
     with pytest.raises(ValueError):
         dash.sched_grid("shift", False, 160, 1, 152)
     assert dash.sched_grid("serial", False, 160, 1, 152) == 152
+    # the packed schedule (and AUTO) take heads wider than the grid in several rounds
+    assert dash.sched_grid("shift_fill", False, 160, 1, 152) == 152
+    assert dash.sched_grid("auto", True, 320, 1, 152) == 152
 
 
 def test_schedule_query_rejects_bad_arguments(L):
