@@ -129,11 +129,12 @@ struct LaunchPlan {
   int sched, workers, grid, packed;
 };
 
-// DASH_SCHED_AUTO: SHIFT_FILL where a shift schedule exists, DESCENDING for a causal mask
-// with an odd tile count (the measured choice; see the header).
+// DASH_SCHED_AUTO: SHIFT_FILL (the measured choice for every mask, head dim and length;
+// see the header).
 int resolve_sched(int sched, int mask, int N) {
-  if (sched != DASH_SCHED_AUTO) return sched;
-  return (mask == DASH_MASK_CAUSAL && (N % 2)) ? DASH_SCHED_DESCENDING : DASH_SCHED_SHIFT_FILL;
+  (void)mask;
+  (void)N;
+  return sched == DASH_SCHED_AUTO ? DASH_SCHED_SHIFT_FILL : sched;
 }
 
 // False when plain SHIFT cannot have every worker of a head resident at once.  SHIFT_FILL
@@ -231,8 +232,6 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   if (!lse || !aligned4(lse)) return DASH_ERR_INVALID;
   const int N = tiles(S);
   const int causal = mask == DASH_MASK_CAUSAL;
-  const bool shift = sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL;
-  if (shift && causal && (N % 2)) return DASH_ERR_UNSUPPORTED;
   const BwdWorkspace need = carve_bwd(nullptr, B, S, H, D);
   if (!workspace || !aligned16(workspace) || workspace_bytes < need.total)
     return DASH_ERR_WORKSPACE;
@@ -394,9 +393,7 @@ dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, 
     if ((st = check_sizes(1, S, H, group, D)) != DASH_OK) return st;
     const int N = tiles(S), rs = resolve_sched(sched, mask, N);
     LaunchPlan plan;
-    if (((rs == DASH_SCHED_SHIFT || rs == DASH_SCHED_SHIFT_FILL) && mask == DASH_MASK_CAUSAL &&
-         (N % 2)) ||
-        !make_plan(rs, mask == DASH_MASK_CAUSAL, N, Hkv, dev.sms, &plan))
+    if (!make_plan(rs, mask == DASH_MASK_CAUSAL, N, Hkv, dev.sms, &plan))
       return DASH_ERR_UNSUPPORTED;
   }
   if (workspace_bytes < dash_attn_bwd_workspace_bytes(1, mx, H, D)) return DASH_ERR_WORKSPACE;
@@ -463,8 +460,6 @@ void dash_debug_set_trace(unsigned long long *buf, int cta) {
 static bool sched_args_ok(int &sched, int mask, int N) {
   if (sched < 0 || sched > DASH_SCHED_AUTO || (mask != 0 && mask != 1) || N <= 0) return false;
   sched = resolve_sched(sched, mask, N);
-  if ((sched == DASH_SCHED_SHIFT || sched == DASH_SCHED_SHIFT_FILL) && mask == 1 && (N % 2))
-    return false;
   return true;
 }
 
@@ -500,7 +495,7 @@ int dash_sched_segments(int sched, int mask, int N, int worker) {
   sched = resolve_sched(sched, mask, N);
   const int W = dash_sched_workers(sched, mask, N);
   if (W < 0 || worker < 0 || worker >= W) return -1;
-  return dash::sched_segments(dash::traversal(sched, mask, N), mask);
+  return dash::sched_segments(dash::traversal(sched, mask, N), mask, N, worker);
 }
 
 int dash_sched_steps(int sched, int mask, int N, int worker, int segment) {

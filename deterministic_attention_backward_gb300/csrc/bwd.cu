@@ -179,7 +179,7 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
       const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
@@ -278,7 +278,7 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg) * p.G;
       // segment prologue: new K_j/V_j and G1 of the first step (the previous step's G3,
@@ -405,7 +405,7 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
       const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
@@ -568,7 +568,7 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
   for (int u = pl.first; u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
     const UnitOrder o = unit_order(p, pl, un);
-    const int nseg = sched_segments(pl.sched, p.causal);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
     for (int seg = 0; seg < nseg; ++seg) {
       const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
       const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
@@ -614,7 +614,7 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
     for (int seg = 0; ok && seg < nseg; ++seg) {
       const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
       const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);

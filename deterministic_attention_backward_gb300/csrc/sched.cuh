@@ -25,10 +25,15 @@
 //      q <  h            : rank = q - kv
 //      q >= h, kv <  h   : rank = (q - h - kv) mod h
 //      q >= h, kv >= h   : rank = kv       (= h + (kv - h), after the h rectangle ones)
+//    Odd N (the pages cover even N only): the head is padded with an empty KV block and
+//    query tile N, the even schedule of Np = N+1 is laid out, and the steps that touch
+//    the padding are dropped.  Worker 0 then owns block 0 alone and worker c >= 1 the
+//    pair (c, N-c); every worker has N steps.  Ranks are the padded schedule's (formulas
+//    above with h = Np/2): its lock-step order, in which the dropped steps are idle
+//    slots.  Run with waits, a head finishes in N+1 steps, as for even N.
 //  ATOMIC: no order; it visits tiles in the shift order (conflict-free and, for the causal
 //    mask, balanced), the most favourable traversal, so that the deterministic schedules
-//    are compared against the fastest non-deterministic backward; odd-N causal falls back
-//    to the SERIAL traversal.
+//    are compared against the fastest non-deterministic backward.
 #pragma once
 
 #if defined(__CUDACC__)
@@ -43,26 +48,35 @@ namespace dash {
 // every CTA of the grid; on the device it runs the kShift traversal with packed ranks.
 enum Sched : int { kAtomic = 0, kSerial = 1, kDescending = 2, kShift = 3, kShiftFill = 4 };
 
-// Which visiting order a schedule uses (ATOMIC borrows the shift order when it exists; the
-// fill mode's shift heads use the shift order).
+// Which visiting order a schedule uses (ATOMIC borrows the shift order; the fill mode's
+// shift heads use the shift order).
 DASH_HD int traversal(int sched, int causal, int N) {
-  if (sched == kShiftFill) return kShift;
-  if (sched != kAtomic) return sched;
-  return (!causal || (N % 2) == 0) ? kShift : kSerial;
+  (void)causal;
+  (void)N;
+  if (sched == kShiftFill || sched == kAtomic) return kShift;
+  return sched;
 }
 
 DASH_HD bool sym_shift(int sched, int causal) { return sched == kShift && causal; }
+// The padded tile count of Symmetric Shift (N rounded up to even) and its half.
+DASH_HD int sym_np(int N) { return N + (N & 1); }
+DASH_HD int sym_h(int N) { return (N + 1) >> 1; }
 
 DASH_HD int sched_workers(int sched, int causal, int N) {
-  return sym_shift(sched, causal) ? N / 2 : N;
+  return sym_shift(sched, causal) ? sym_h(N) : N;
 }
-DASH_HD int sched_segments(int sched, int causal) { return sym_shift(sched, causal) ? 2 : 1; }
+// Segments of worker w: two for a Symmetric Shift pair, one for worker 0 of an odd N (its
+// partner would be the padding block).
+DASH_HD int sched_segments(int sched, int causal, int N, int w) {
+  if (!sym_shift(sched, causal)) return 1;
+  return ((N & 1) && w == 0) ? 1 : 2;
+}
 DASH_HD int seg_kv(int sched, int causal, int N, int w, int seg) {
-  return (sym_shift(sched, causal) && seg == 1) ? N - 1 - w : w;
+  return (sym_shift(sched, causal) && seg == 1) ? sym_np(N) - 1 - w : w;
 }
 DASH_HD int seg_steps(int sched, int causal, int N, int w, int seg) {
   if (!causal) return N;
-  if (sched == kShift) return seg == 0 ? N - w : w + 1;
+  if (sched == kShift) return seg == 0 ? N - w : w + 1 - (N & 1);
   return N - w;
 }
 DASH_HD int step_q(int sched, int causal, int N, int w, int seg, int t) {
@@ -74,8 +88,11 @@ DASH_HD int step_q(int sched, int causal, int N, int w, int seg, int t) {
         int q = w + t;
         return q >= N ? q - N : q;
       }
-      const int h = N >> 1;
-      if (seg == 1) return N - 1 - t;
+      // t is the step among those kept; for odd N, skip the padded schedule's steps on
+      // the padding tile (step h-1-w of segment 0, step 0 of segment 1)
+      const int odd = N & 1, Np = sym_np(N), h = sym_h(N);
+      if (seg == 1) return Np - 1 - (t + odd);
+      if (odd && t >= h - 1 - w) ++t;
       if (t < h) {
         int r = w + t;
         r = r >= h ? r - h : r;
@@ -83,7 +100,7 @@ DASH_HD int step_q(int sched, int causal, int N, int w, int seg, int t) {
       }
       return w + (t - h);
     }
-    default:  // kAtomic, kSerial
+    default:  // kSerial
       return causal ? w + t : t;
   }
 }
@@ -93,7 +110,7 @@ DASH_HD int dq_rank(int sched, int causal, int N, int q, int kv) {
     int r = q - kv;
     return r < 0 ? r + N : r;
   }
-  const int h = N >> 1;
+  const int h = sym_h(N);
   if (q < h) return q - kv;
   if (kv < h) {
     int r = q - h - kv;
@@ -113,17 +130,19 @@ DASH_HD int dq_rank(int sched, int causal, int N, int q, int kv) {
 
 // Worker (within its head) that owns KV block kv under the shift schedule.
 DASH_HD int shift_worker_of(int causal, int N, int kv) {
-  return (causal && kv >= (N >> 1)) ? N - 1 - kv : kv;
+  return (causal && kv >= sym_h(N)) ? sym_np(N) - 1 - kv : kv;
 }
 // Step, within its worker's program, at which the shift worker owning block kv visits
-// query tile q; -1 if the tile is masked for that block.
+// query tile q; -1 if the tile is masked for that block (or kv is the padding block).
+// For the causal mask this is the step of the padded (even) schedule, whose order is the
+// accumulation order.
 DASH_HD int shift_visit_step(int causal, int N, int kv, int q) {
   if (!causal) {
     const int t = q - kv;
     return t < 0 ? t + N : t;
   }
   if (q < kv) return -1;
-  const int h = N >> 1;
+  const int h = sym_h(N), Np = sym_np(N);
   if (kv < h) {  // worker c = kv, first segment
     if (q >= h) {
       const int t = q - h - kv;
@@ -131,8 +150,8 @@ DASH_HD int shift_visit_step(int causal, int N, int kv, int q) {
     }
     return h + (q - kv);
   }
-  const int c = N - 1 - kv;  // worker c, second segment (block N-1-c)
-  return (N - c) + (N - 1 - q);
+  const int c = Np - 1 - kv;  // worker c, second segment (block Np-1-c)
+  return (Np - c) + (Np - 1 - q);
 }
 // The phase [lo, hi) of worker w of head hd: the workers of hd in w's round.
 DASH_HD void packed_phase(int W, int P, int hd, int w, int *lo, int *hi) {
@@ -151,7 +170,7 @@ DASH_HD int packed_count_in_phase(int causal, int N, int q, int kv, int c_begin,
     const int t1 = shift_visit_step(causal, N, c, q);
     if (t1 >= 0 && t1 < tme) ++n;
     if (causal) {
-      const int t2 = shift_visit_step(causal, N, N - 1 - c, q);
+      const int t2 = shift_visit_step(causal, N, sym_np(N) - 1 - c, q);
       if (t2 >= 0 && t2 < tme) ++n;
     }
   }
@@ -161,13 +180,13 @@ DASH_HD int packed_count_in_phase(int causal, int N, int q, int kv, int c_begin,
 DASH_HD int packed_count_before(int causal, int N, int q, int lo) {
   if (!causal) return lo;
   const int a = lo < q + 1 ? lo : q + 1;             // blocks c <= q, c < lo
-  const int b = lo - (N - 1 - q);                    // blocks N-1-c <= q, c < lo
+  const int b = lo - (sym_np(N) - 1 - q);            // blocks Np-1-c <= q, c < lo
   return a + (b > 0 ? b : 0);
 }
 // Rank of block kv in dQ tile q of head hd (full mask in closed form; the causal count is
 // the same definition evaluated over the phase's workers).
 DASH_HD int packed_rank(int causal, int N, int P, int hd, int q, int kv) {
-  const int W = causal ? (N >> 1) : N;
+  const int W = causal ? sym_h(N) : N;
   int lo, hi;
   packed_phase(W, P, hd, shift_worker_of(causal, N, kv), &lo, &hi);
   if (!causal) {

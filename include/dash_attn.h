@@ -52,8 +52,7 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *  DASH_SCHED_ATOMIC     -- non-deterministic reference: dQ partials are added with
  *                           unordered atomics (the "non-deterministic counterpart" of
  *                           section 1).  It visits tiles in the SHIFT order (cyclic /
- *                           symmetric; SERIAL for a causal mask with odd N), the fastest
- *                           traversal, so that it is the speed reference for the
+ *                           symmetric), the fastest traversal, so that it is the speed reference for the
  *                           deterministic schedules.
  *  DASH_SCHED_SERIAL     -- deterministic baseline: the worker owning KV block j visits
  *                           query tiles in ascending order; every dQ tile adds the KV
@@ -66,9 +65,13 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           tile q adds KV blocks q, q-1, .., q+1 (mod N).  Causal mask:
  *                           Symmetric Shift -- the worker c owns KV blocks c and N-1-c,
  *                           first the dense lower-left rectangle, then the folded
- *                           triangle; requires an even N.
+ *                           triangle.  Odd N (not covered by the pages): laid out as the
+ *                           even schedule of N+1 tiles with the steps on the padding tile
+ *                           dropped -- worker 0 owns block 0 alone, worker c >= 1 the
+ *                           pair (c, N-c), (N+1)/2 workers of N steps each; the
+ *                           accumulation order is the padded schedule's lock-step order.
  *  DASH_SCHED_SHIFT_FILL -- packed Shift Scheduling: the shift workers of all heads (W per
- *                           head: N, or N/2 for the causal mask) are dealt round-robin,
+ *                           head: N, or ceil(N/2) for the causal mask) are dealt round-robin,
  *                           head-major, to every SM.  When W does not divide the SM count
  *                           a head's workers can fall into two consecutive rounds; such a
  *                           head runs as two lock-step phases, and each of its dQ tiles adds
@@ -85,9 +88,7 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           leave the choice to the user.  Measured over every configuration
  *                           of the benchmark (full and causal masks, D = 64 and 128,
  *                           S = 512 .. 16384, GQA 4:1), SHIFT_FILL is the fastest or within
- *                           1 % of it wherever a shift schedule exists; for a causal mask
- *                           with an odd tile count (no Symmetric Shift) DESCENDING beats
- *                           SERIAL.  So AUTO = SHIFT_FILL, or DESCENDING for causal odd N. */
+ *                           1 % of it (odd tile counts included).  So AUTO = SHIFT_FILL. */
 typedef enum {
   DASH_SCHED_ATOMIC = 0,
   DASH_SCHED_SERIAL = 1,
@@ -140,8 +141,8 @@ size_t dash_attn_bwd_workspace_bytes(int B, int S, int H, int D);
  *   dq [B,S,H,D]; dk, dv [B,S,H/group,D]                       (outputs, overwritten)
  *   workspace: >= dash_attn_bwd_workspace_bytes(B,S,H,D) bytes, caller-owned, contents
  *   need not be initialised; one workspace must not be used by two calls that may run
- *   concurrently.  Requires N <= number of SMs for DASH_SCHED_SHIFT (all workers of
- *   a head run concurrently); the shift schedules with a causal mask require an even N. */
+ *   concurrently.  DASH_SCHED_SHIFT requires a head's workers (N; ceil(N/2) for the
+ *   causal mask) to fit on the SMs at once: they wait on one another. */
 dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
                             int B, int S, int H, int group, int D, float scale,

@@ -35,7 +35,13 @@ Readings of the pages (where they are silent or loose):
   rectangle (q >= h, kv < h) cyclically; phase 2 covers the folded triangle.  The
   pages give no exact step order, so the one below is constructed to be conflict-free
   and to finish block c before starting block N-1-c.  The accumulation order of a tile
-  is its lock-step order.  N must be even.
+  is its lock-step order.
+* SYMSHIFT with an odd N (the pages pair blocks i and N-1-i, which needs an even N; they
+  say nothing of odd N): append an empty KV block and query tile N, lay out the even
+  schedule of N+1 tiles, and drop every step that touches the padding.  The dropped
+  steps stay idle slots of the lock step, so a tile's accumulation order is still its
+  lock-step order.  Worker 0 is left with block 0 alone and worker c >= 1 with the pair
+  (c, N-c); each has N steps.
 """
 from __future__ import annotations
 
@@ -49,40 +55,60 @@ def allowed(causal: bool, q: int, kv: int) -> bool:
 
 
 def num_workers(sched: str, causal: bool, N: int) -> int:
-    return N // 2 if sched == SYMSHIFT else N
+    return (N + 1) // 2 if sched == SYMSHIFT else N
+
+
+def _symshift_even(N: int, c: int) -> list[tuple[int, int]]:
+    """Worker c's (kv, q) steps of the Symmetric Shift for an even N."""
+    h = N // 2
+    out = [(c, h + (c + t) % h) for t in range(h)]               # phase 1: rectangle
+    for t in range(h + 1):                                       # phase 2: folded triangle
+        p = (c + 1 + t) % (h + 1)
+        out.append((c, p - 1) if p >= c + 1 else (N - 1 - c, N - 1 - p))
+    return out
+
+
+def timed_visits(sched: str, causal: bool, N: int, u: int) -> list[tuple[int, int, int]]:
+    """(slot, kv, q) for worker u in processing order: slot is the lock-step time."""
+    if sched == SERIAL:
+        seq = [(u, q) for q in range(N) if allowed(causal, q, u)]
+    elif sched == DESCENDING:
+        seq = [(u, q) for q in reversed(range(N)) if allowed(causal, q, u)]
+    elif sched == SHIFT:
+        if causal:
+            raise ValueError("cyclic shift is the full-mask schedule; causal uses symshift")
+        seq = [(u, (u + t) % N) for t in range(N)]
+    elif sched == SYMSHIFT:
+        if not causal:
+            raise ValueError("symmetric shift is the causal-mask schedule")
+        if N % 2 == 0:
+            seq = _symshift_even(N, u)
+        else:  # odd N: the even schedule of N+1 tiles; padding steps become idle slots
+            return [(t, kv, q) for t, (kv, q) in enumerate(_symshift_even(N + 1, u))
+                    if kv < N and q < N]
+    else:
+        raise ValueError(sched)
+    return [(t, kv, q) for t, (kv, q) in enumerate(seq)]
 
 
 def visits(sched: str, causal: bool, N: int, u: int) -> list[tuple[int, int]]:
     """(kv, q) pairs processed by worker u, in processing order."""
-    if sched == SERIAL:
-        return [(u, q) for q in range(N) if allowed(causal, q, u)]
-    if sched == DESCENDING:
-        return [(u, q) for q in reversed(range(N)) if allowed(causal, q, u)]
-    if sched == SHIFT:
-        if causal:
-            raise ValueError("cyclic shift is the full-mask schedule; causal uses symshift")
-        return [(u, (u + t) % N) for t in range(N)]
-    if sched == SYMSHIFT:
-        if not causal or N % 2:
-            raise ValueError("symmetric shift needs a causal mask and an even N")
-        h, c = N // 2, u
-        out = [(c, h + (c + t) % h) for t in range(h)]           # phase 1: rectangle
-        for t in range(h + 1):                                   # phase 2: folded triangle
-            p = (c + 1 + t) % (h + 1)
-            out.append((c, p - 1) if p >= c + 1 else (N - 1 - c, N - 1 - p))
-        return out
-    raise ValueError(sched)
+    return [(kv, q) for _, kv, q in timed_visits(sched, causal, N, u)]
+
+
+def _arrivals(sched: str, causal: bool, N: int) -> dict[int, list[tuple[int, int]]]:
+    arrivals: dict[int, list[tuple[int, int]]] = {q: [] for q in range(N)}
+    for u in range(num_workers(sched, causal, N)):
+        for t, kv, q in timed_visits(sched, causal, N, u):
+            arrivals[q].append((t, kv))
+    return arrivals
 
 
 def reduction_order(sched: str, causal: bool, N: int) -> dict[int, list[int]]:
     """dQ tile q -> KV blocks in the order their partials are added."""
     if sched in (SERIAL, DESCENDING):
         return {q: [kv for kv in range(N) if allowed(causal, q, kv)] for q in range(N)}
-    arrivals: dict[int, list[tuple[int, int]]] = {q: [] for q in range(N)}
-    for u in range(num_workers(sched, causal, N)):
-        for t, (kv, q) in enumerate(visits(sched, causal, N, u)):
-            arrivals[q].append((t, kv))
-    return {q: [kv for _, kv in sorted(a)] for q, a in arrivals.items()}
+    return {q: [kv for _, kv in sorted(a)] for q, a in _arrivals(sched, causal, N).items()}
 
 
 def rank_table(sched: str, causal: bool, N: int) -> dict[tuple[int, int], int]:
@@ -92,10 +118,7 @@ def rank_table(sched: str, causal: bool, N: int) -> dict[tuple[int, int], int]:
 
 
 def conflict_free(sched: str, causal: bool, N: int) -> bool:
-    arrivals: dict[int, list[tuple[int, int]]] = {q: [] for q in range(N)}
-    for u in range(num_workers(sched, causal, N)):
-        for t, (kv, q) in enumerate(visits(sched, causal, N, u)):
-            arrivals[q].append((t, kv))
+    arrivals = _arrivals(sched, causal, N)
     order = reduction_order(sched, causal, N)
     for q, a in arrivals.items():
         a.sort()
@@ -158,10 +181,10 @@ def packed_reduction_order(sched: str, causal: bool, N: int, heads: int, P: int)
     """(head, q) -> KV blocks in the order their partials are added."""
     W = num_workers(sched, causal, N)
     rounds = packed_rounds(sched, causal, N, heads, P)
-    steps_per_round = max(len(visits(sched, causal, N, w)) for w in range(W))
+    steps_per_round = 1 + max(t for w in range(W) for t, _, _ in timed_visits(sched, causal, N, w))
     arrivals: dict = {}
     for (hd, w), r in rounds.items():
-        for t, (kv, q) in enumerate(visits(sched, causal, N, w)):
+        for t, kv, q in timed_visits(sched, causal, N, w):
             arrivals.setdefault((hd, q), []).append((r * steps_per_round + t, kv))
     out = {}
     for key, a in arrivals.items():

@@ -58,8 +58,8 @@ def test_argument_errors_are_synchronous(L):
                         1, 512, 3, 2, 64, 0.0, 0, 1, null, 0, null)
     assert c == 1                                                # H % group
     fake = 1 << 20                                               # never dereferenced
-    c = L.dash_attn_bwd(*([fake] * 9), 1, 384, 2, 1, 64, 0.0, 1, 3, fake, 1 << 30, null)
-    assert c == 2                                                # symmetric shift, odd N
+    c = L.dash_attn_bwd(*([fake] * 9), 1, 384, 2, 1, 64, 0.0, 1, 6, fake, 1 << 30, null)
+    assert c == 1                                                # unknown schedule
     c = L.dash_attn_bwd(*([fake] * 9), 1, 512, 2, 1, 64, 0.0, 1, 3, fake, 16, null)
     assert c == 5                                                # workspace too small
     c = L.dash_attn_bwd(*([fake + 4] + [fake] * 8), 1, 512, 2, 1, 64, 0.0, 1, 3, fake, 1 << 30,
@@ -72,7 +72,7 @@ SCHEDS = [("serial", sc.SERIAL), ("descending", sc.DESCENDING), ("atomic", None)
           ("shift", None), ("shift_fill", None)]
 
 
-@pytest.mark.parametrize("N", [2, 4, 6, 8, 16, 64, 128])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 33, 64, 127, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("name,oracle_name", SCHEDS)
 def test_library_schedule_equals_oracle(L, name, oracle_name, causal, N):
@@ -90,20 +90,28 @@ def test_library_schedule_equals_oracle(L, name, oracle_name, causal, N):
                 assert r == ranks[(q, kv)]
 
 
-def test_atomic_odd_causal_falls_back_to_serial_traversal(L):
-    table = dash.sched_table("atomic", True, 5)
-    flat = [[(kv, q) for seg in segs for kv, q, _ in seg] for segs in table]
-    assert flat == [sc.visits(sc.SERIAL, True, 5, w) for w in range(5)]
+def test_odd_symmetric_shift_segments(L):
+    """Odd N: worker 0 has one segment (block 0), every other worker two (c, then N-c),
+    all of N steps."""
+    N = 7
+    table = dash.sched_table("shift", True, N)
+    assert len(table) == 4
+    assert len(table[0]) == 1 and [kv for kv, _, _ in table[0][0]] == [0] * N
+    for c in range(1, 4):
+        assert [len(seg) for seg in table[c]] == [N - c, c]
+        assert {kv for kv, _, _ in table[c][1]} == {N - c}
 
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N,heads,P", [(8, 5, 12), (8, 3, 8), (16, 4, 24), (4, 9, 10), (32, 3, 38),
                                        (32, 64, 152), (64, 8, 152), (16, 20, 152),
-                                       (16, 3, 5), (32, 2, 10), (64, 1, 31), (24, 2, 7)])
+                                       (16, 3, 5), (32, 2, 10), (64, 1, 31), (24, 2, 7),
+                                       (5, 7, 4), (9, 3, 5), (33, 5, 38), (127, 3, 152),
+                                       (3, 40, 152), (31, 2, 7)])
 def test_packed_ranks_equal_oracle(L, causal, N, heads, P):
     """The library's packed-shift ranks equal the oracle's lock-step simulation of the
     workers dealt round-robin to P CTAs, also when a head has more workers than CTAs."""
-    W = N // 2 if causal else N
+    W = (N + 1) // 2 if causal else N
     if P > heads * W:
         P = heads * W
     order = sc.packed_reduction_order(sc.SYMSHIFT if causal else sc.SHIFT, causal, N, heads, P)
@@ -129,7 +137,8 @@ def test_grid_sizes(L, causal):
 
 
 def test_schedule_query_rejects_bad_arguments(L):
-    assert L.dash_sched_workers(3, 1, 5) == -1
+    assert L.dash_sched_workers(3, 1, 0) == -1
+    assert L.dash_sched_workers(3, 1, 5) == 3                   # odd N: ceil(N/2) workers
     assert L.dash_sched_workers(7, 0, 4) == -1
     assert L.dash_sched_step(1, 0, 4, 0, 0, 4, None, None, None) == -1
 
@@ -137,9 +146,9 @@ def test_schedule_query_rejects_bad_arguments(L):
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_auto_schedule_resolution(L, causal, N):
-    """AUTO runs the packed shift schedule wherever a shift schedule exists, Descending
-    Q-Tile Iteration for a causal mask with an odd tile count; other schedules pass through."""
-    want = "descending" if (causal and N % 2) else "shift_fill"
+    """AUTO runs the packed shift schedule for every mask and tile count; other schedules
+    pass through."""
+    want = "shift_fill"
     assert dash.sched_resolve("auto", causal, N) == want
     for name in ("atomic", "serial", "descending"):
         assert dash.sched_resolve(name, causal, N) == name

@@ -65,11 +65,11 @@ def test_full_size_sampled_rows_match_oracle(dash, cfg):
         close(f"{name} {s} dV", dv[b, kr, g], sv)
 
 
-@pytest.mark.parametrize("causal,S", [(False, 160 * 128), (True, 320 * 128)])
+@pytest.mark.parametrize("causal,S", [(False, 160 * 128), (True, 320 * 128), (True, 319 * 128)])
 def test_heads_wider_than_the_grid(dash, causal, S):
-    """More shift workers per head than SMs (full: N = 160; causal: N/2 = 160 pairs): the
-    packed schedule (and AUTO) runs the head in several rounds; sampled rows match the
-    oracle and repeats are bit-identical."""
+    """More shift workers per head than SMs (full: N = 160; causal: 160 pairs, also for
+    the odd N = 319): the packed schedule (and AUTO) runs the head in several rounds;
+    sampled rows match the oracle and repeats are bit-identical."""
     B, H, Hkv, D = 1, 2, 1, 64
     host = make_qkv_do(B, S, H, Hkv, D, seed=4)
     q, k, v, do = (t.cuda() for t in host)

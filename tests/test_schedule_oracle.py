@@ -36,7 +36,7 @@ def test_descending_matches_pages_reversal():
     assert sc.reduction_order(sc.DESCENDING, False, 4) == sc.reduction_order(sc.SERIAL, False, 4)
 
 
-CASES = [(s, c, n) for n in (2, 4, 6, 8, 16) for s, c in
+CASES = [(s, c, n) for n in (1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 17) for s, c in
          ((sc.SERIAL, False), (sc.SERIAL, True), (sc.DESCENDING, False), (sc.DESCENDING, True),
           (sc.SHIFT, False), (sc.SYMSHIFT, True))]
 
@@ -56,15 +56,17 @@ def test_every_allowed_tile_visited_once(sched, causal, N):
 @pytest.mark.parametrize("sched,causal,N", CASES)
 def test_conflict_freedom(sched, causal, N):
     """Shift schedules are conflict-free in lock step (section 2.2 B); the serialized
-    orders are not (every worker wants the same tile at the same step)."""
-    assert sc.conflict_free(sched, causal, N) == (sched in (sc.SHIFT, sc.SYMSHIFT))
+    orders are not (every worker wants the same tile at the same step; a single tile is
+    trivially conflict-free)."""
+    assert sc.conflict_free(sched, causal, N) == (sched in (sc.SHIFT, sc.SYMSHIFT) or N == 1)
 
 
-@pytest.mark.parametrize("N", [2, 4, 8, 16])
+@pytest.mark.parametrize("N", [2, 3, 4, 5, 8, 9, 16, 17])
 def test_critical_paths(N):
     """Unit-step critical paths.  Serialized baseline: 2N-1 (the pipeline bubbles of
     section 1).  Descending helps causal masks only (section 2.2 A); Shift reaches the
-    lower bound N for full masks; Symmetric Shift needs N+1 steps on N/2 workers."""
+    lower bound N for full masks; Symmetric Shift needs N+1 steps on ceil(N/2) workers
+    (odd N: the padded schedule, its dropped steps closed up by the waits)."""
     assert sc.critical_path(sc.SERIAL, False, N) == 2 * N - 1
     assert sc.critical_path(sc.DESCENDING, False, N) == 2 * N - 1
     assert sc.critical_path(sc.SHIFT, False, N) == N
@@ -88,15 +90,45 @@ def test_symshift_balanced_and_one_block_at_a_time(N):
         assert all(q >= N // 2 for _, q in seq[:N // 2])      # phase 1: lower-left rectangle
 
 
-def test_symshift_rejects_odd_or_full():
-    with pytest.raises(ValueError):
-        sc.visits(sc.SYMSHIFT, True, 5, 0)
+@pytest.mark.parametrize("N", [1, 3, 5, 7, 9, 31])
+def test_odd_symshift_balanced_and_one_block_at_a_time(N):
+    """Odd N: (N+1)/2 workers of N steps each (N(N+1)/2 tiles in all); worker 0 runs block
+    0 alone, worker c >= 1 finishes block c before it starts block N-c."""
+    W = sc.num_workers(sc.SYMSHIFT, True, N)
+    assert W == (N + 1) // 2
+    for c in range(W):
+        kvs = [kv for kv, _ in sc.visits(sc.SYMSHIFT, True, N, c)]
+        assert len(kvs) == N
+        if c == 0:
+            assert kvs == [0] * N
+        else:
+            assert kvs == [c] * (N - c) + [N - c] * c
+
+
+def test_odd_symshift_matches_hand_worked_example():
+    gold = {}
+    with open(os.path.join(GOLDEN, "symshift_causal_N5.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                w, rest = line.split(":")
+                gold[int(w)] = [tuple(int(x) for x in p.split(",")) for p in rest.split()]
+    assert set(gold) == {0, 1, 2}
+    for c, pairs in gold.items():
+        assert sc.visits(sc.SYMSHIFT, True, 5, c) == pairs
+    order = sc.reduction_order(sc.SYMSHIFT, True, 5)
+    # lock-step slots (padding steps idle): tile 4 gets kv 1, 0, 2 in phase 1, then 3, 4
+    assert order[1] == [1, 0] and order[3] == [0, 2, 1, 3] and order[4] == [1, 0, 2, 3, 4]
+
+
+def test_symshift_rejects_full():
     with pytest.raises(ValueError):
         sc.visits(sc.SYMSHIFT, False, 4, 0)
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N,heads,P", [(8, 5, 12), (8, 3, 8), (16, 4, 24), (4, 9, 10), (32, 3, 38)])
+@pytest.mark.parametrize("N,heads,P", [(8, 5, 12), (8, 3, 8), (16, 4, 24), (4, 9, 10), (32, 3, 38),
+                                       (5, 4, 7), (9, 3, 10)])
 def test_packed_shift_is_conflict_free_and_reduces_to_shift(causal, N, heads, P):
     sched = sc.SYMSHIFT if causal else sc.SHIFT
     order = sc.packed_reduction_order(sched, causal, N, heads, P)
