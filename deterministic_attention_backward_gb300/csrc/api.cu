@@ -142,7 +142,7 @@ int resolve_sched(int sched, int mask, int N) {
 // the grid simply spans more rounds.
 bool make_plan(int sched, int causal, int N, int heads, int sms, LaunchPlan *pl) {
   pl->sched = dash::traversal(sched, causal, N);
-  pl->workers = dash::sched_workers(pl->sched, causal, N);
+  pl->workers = dash::sched_workers(pl->sched, causal, N, N & 1);
   const long long total = (long long)heads * pl->workers;
   pl->grid = (int)(total < sms ? total : sms);
   pl->packed = sched == DASH_SCHED_SHIFT_FILL;
@@ -297,8 +297,9 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   p.trace_cta = 0;
 #endif
   if ((stages & DASH_BWD_TILES) &&
-      dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC, tq, tk, tv, tdo, p, plan.grid, s) !=
-          cudaSuccess)
+      dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC,
+                       causal && (N & 1) && plan.sched == dash::kShift, tq, tk, tv, tdo, p,
+                       plan.grid, s) != cudaSuccess)
     return DASH_ERR_CUDA;
   if ((stages & DASH_BWD_EPILOGUE) &&
       dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, s) !=
@@ -481,28 +482,28 @@ int dash_sched_packed_rank(int mask, int N, int heads, int grid, int head, int q
   if (!sched_args_ok(fill, mask, N) || heads <= 0 || head < 0 ||
       head >= heads || q < 0 || q >= N || kv < 0 || kv >= N || (mask && kv > q))
     return -1;
-  const int W = dash::sched_workers(dash::kShift, mask, N);
+  const int W = dash::sched_workers(dash::kShift, mask, N, N & 1);
   if (grid < 1 || grid > heads * W) return -1;
-  return dash::packed_rank(mask, N, grid, head, q, kv);
+  return dash::packed_rank(mask, N, grid, head, q, kv, N & 1);
 }
 
 int dash_sched_workers(int sched, int mask, int N) {
   if (!sched_args_ok(sched, mask, N)) return -1;
-  return dash::sched_workers(dash::traversal(sched, mask, N), mask, N);
+  return dash::sched_workers(dash::traversal(sched, mask, N), mask, N, N & 1);
 }
 
 int dash_sched_segments(int sched, int mask, int N, int worker) {
   sched = resolve_sched(sched, mask, N);
   const int W = dash_sched_workers(sched, mask, N);
   if (W < 0 || worker < 0 || worker >= W) return -1;
-  return dash::sched_segments(dash::traversal(sched, mask, N), mask, N, worker);
+  return dash::sched_segments(dash::traversal(sched, mask, N), mask, N, worker, N & 1);
 }
 
 int dash_sched_steps(int sched, int mask, int N, int worker, int segment) {
   sched = resolve_sched(sched, mask, N);
   const int nseg = dash_sched_segments(sched, mask, N, worker);
   if (nseg < 0 || segment < 0 || segment >= nseg) return -1;
-  return dash::seg_steps(dash::traversal(sched, mask, N), mask, N, worker, segment);
+  return dash::seg_steps(dash::traversal(sched, mask, N), mask, N, worker, segment, N & 1);
 }
 
 int dash_sched_step(int sched, int mask, int N, int worker, int segment, int step, int *kv,
@@ -511,12 +512,12 @@ int dash_sched_step(int sched, int mask, int N, int worker, int segment, int ste
   const int n = dash_sched_steps(sched, mask, N, worker, segment);
   if (n < 0 || step < 0 || step >= n) return -1;
   const int t = dash::traversal(sched, mask, N);
-  const int kvb = dash::seg_kv(t, mask, N, worker, segment);
-  const int qt = dash::step_q(t, mask, N, worker, segment, step);
+  const int kvb = dash::seg_kv(t, mask, N, worker, segment, N & 1);
+  const int qt = dash::step_q(t, mask, N, worker, segment, step, N & 1);
   if (kv) *kv = kvb;
   if (q) *q = qt;
   // ATOMIC adds in no fixed order; report the position the traversal would give
-  if (rank) *rank = dash::dq_rank(t, mask, N, qt, kvb);
+  if (rank) *rank = dash::dq_rank(t, mask, N, qt, kvb, N & 1);
   return 0;
 }
 

@@ -58,6 +58,10 @@
 namespace dash {
 namespace {
 
+// Depth of the ring of mbarriers through which the semaphore poller hands a dQ tile's turn
+// to the epilogue (D = 128, ordered variant).
+constexpr int kTurns = 4;
+
 template <int D, bool DET>
 struct BwdLayout {
   static constexpr int kStages = (D == 64) ? (DET ? 4 : 3) : 2;
@@ -80,7 +84,12 @@ struct BwdLayout {
   static constexpr int offLSE = offStg + kStgBytes;
   static constexpr int offDVEC = offLSE + kStages * kTile * 4;
   static constexpr int offBar = offDVEC + kStages * kTile * 4;
-  static constexpr int kNumBars = 2 * kStages + 15;
+  // D = 128, ordered: the poller hands each turn to the epilogue through an mbarrier ring,
+  // on which the epilogue's thread waits suspended instead of spinning on a shared-memory
+  // counter, so it adds no shared-memory loads beside the softmax-gradient warps' traffic
+  // (measured: +3 % at D = 128).  At D = 64 the counter measured faster.
+  static constexpr bool kTurnRing = DET && D == 128;
+  static constexpr int kNumBars = 2 * kStages + 15 + (kTurnRing ? 2 * kTurns : 0);
   static constexpr int offMisc = offBar + kNumBars * 8;
   static constexpr int kBytes = offMisc + 32;
   static constexpr uint32_t tS = 0, tDP = 128, tDK = 256, tDV = 256 + D;
@@ -142,7 +151,7 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams &p, const Plan &pl, 
 template <int D, bool DET>
 struct Bars {
   uint64_t *full, *empty, *kv_full, *kv_empty, *s_full, *p_ready, *dp_full, *pds, *g5_done,
-      *dq_empty, *dkv_full, *dkv_empty, *drain;
+      *dq_empty, *dkv_full, *dkv_empty, *drain, *turn_full, *turn_empty;
   __device__ explicit Bars(uint8_t *smem) {
     using L = BwdLayout<D, DET>;
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + L::offBar);
@@ -160,12 +169,14 @@ struct Bars {
     dkv_full = b + 12;
     dkv_empty = b + 13;
     drain = b + 14;
+    turn_full = L::kTurnRing ? b + 15 : nullptr;  // [kTurns]: the step's semaphore reached its rank
+    turn_empty = L::kTurnRing ? b + 15 + kTurns : nullptr;  // [kTurns]: the step was released
   }
 };
 
 // ---------------------------------------------------------------------------------------
 // TMA producer: the whole warp runs the loop; one elected lane issues the copies.
-template <int D, bool DET>
+template <int D, bool DET, int ODD>
 __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                              const CUtensorMap *tdo, const BwdParams &p, uint8_t *smem,
                              const Bars<D, DET> &bar, const Abort &ab) {
@@ -179,10 +190,10 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
+      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg, ODD);
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD);
       if (!mbar_wait_warp(bar.kv_empty, (seg_it & 1) ^ 1, ab)) {
         ok = false;
         break;
@@ -204,7 +215,7 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
       // GQA: the G query heads of a step are visited back to back, so every head keeps the
       // schedule's lock step
       for (int t = 0; ok && t < nsteps; ++t) {
-        const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
+        const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t, ODD);
         for (int g = 0; g < p.G; ++g) {
           const int h = un.hkv * p.G + g;
           const int s = it % L::kStages;
@@ -248,7 +259,7 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
 // warp-uniform); one elected lane issues each tcgen05 instruction.  Once the
 // softmax-gradient warps have written P^T over the current S^T columns, G3 and then the
 // next step's S^T product are issued, so both run while those warps compute dS.
-template <int D, bool DET>
+template <int D, bool DET, int ODD>
 __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
                         const Abort &ab) {
   using L = BwdLayout<D, DET>;
@@ -278,9 +289,9 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg) * p.G;
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD) * p.G;
       // segment prologue: new K_j/V_j and G1 of the first step (the previous step's G3,
       // the last reader of the S^T columns, was issued before and runs first)
       if (!mbar_wait_warp(bar.kv_full, seg_it & 1, ab) ||
@@ -389,7 +400,7 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
 // columns just read (the A operand of G3); then, when dP^T has arrived, compute
 // dS^T = P^T (dP^T - Dvec) chunk by chunk and write it (bf16x2) back over the dP^T columns
 // just read; dS also goes to shared memory for G5.
-template <int D, bool DET>
+template <int D, bool DET, int ODD>
 __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tmem,
                                  const Bars<D, DET> &bar, const Abort &ab) {
   using L = BwdLayout<D, DET>;
@@ -405,13 +416,13 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
+      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg, ODD);
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD);
       for (int t = 0; ok && t < nsteps; ++t) {
         for (int g = 0; g < p.G; ++g, ++it) {
-          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
+          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t, ODD);
           const bool diag = p.causal && (q == kv);
           // a key row past S (partial last tile) reads zeros; its P is set to zero so that
           // nothing of it (not even an overflowing exp of -LSE) reaches dS
@@ -541,47 +552,57 @@ __device__ __forceinline__ UnitOrder unit_order(const BwdParams &p, const Plan &
   o.split = p.packed && (o.ph_hi - o.ph_lo) != pl.W;
   return o;
 }
+template <int ODD>
 __device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, const UnitOrder &o,
                                          int q, int kv, int lane) {
-  if (!o.split) return dq_rank(pl.sched, p.causal, p.N, q, kv);
-  if (!p.causal) return packed_rank(0, p.N, (int)gridDim.x, o.hd, q, kv);
+  if (!o.split) return dq_rank(pl.sched, p.causal, p.N, q, kv, ODD);
+  if (!p.causal) return packed_rank(0, p.N, (int)gridDim.x, o.hd, q, kv, 0);
   const int per = (o.ph_hi - o.ph_lo + 31) >> 5;
   const int cb = o.ph_lo + lane * per;
   const int ce = cb + per < o.ph_hi ? cb + per : o.ph_hi;
-  const int n = cb < ce ? packed_count_in_phase(1, p.N, q, kv, cb, ce) : 0;
-  return packed_count_before(1, p.N, q, o.ph_lo) + (int)__reduce_add_sync(0xffffffffu, n);
+  const int n = cb < ce ? packed_count_in_phase(1, p.N, q, kv, cb, ce, ODD) : 0;
+  return packed_count_before(1, p.N, q, o.ph_lo, ODD) + (int)__reduce_add_sync(0xffffffffu, n);
 }
 
 // Semaphore poller (warp 3, deterministic modes): walks this CTA's steps in the
 // epilogue's order and, for each, waits until the step's dQ tile semaphore equals the
-// step's rank, then publishes the number of steps acquired so far in shared memory.  The
-// L2 round trips of the polling thus overlap the computation of the dQ partial instead
-// of following its drain.  It runs ahead of the epilogue by any number of steps; that is
-// safe because a tile's count only grows.
-template <int D, bool DET>
+// step's rank, then hands the turn to the epilogue: at D = 128 by arriving on the step's
+// slot of the turn ring (it runs at most kTurns steps ahead), at D = 64 by publishing the
+// number of steps acquired so far in shared memory (any number ahead; safe because a
+// tile's count only grows).  The L2 round trips of the polling thus overlap the
+// computation of the dQ partial instead of following its drain.
+template <int D, bool DET, int ODD>
 __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &ab) {
   using L = BwdLayout<D, DET>;
   const int lane = lane_id();
   uint32_t *seen = reinterpret_cast<uint32_t *>(smem + L::offMisc + 16);
+  const Bars<D, DET> bar(smem);
   uint32_t it = 0;
   const Plan pl = cta_plan(p);
   for (int u = pl.first; u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
     const UnitOrder o = unit_order(p, pl, un);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
     for (int seg = 0; seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
+      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg, ODD);
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD);
       for (int t = 0; t < nsteps; ++t) {
-        const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
-        const int rank = step_rank(p, pl, o, q, kv, lane);
+        const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t, ODD);
+        const int rank = step_rank<ODD>(p, pl, o, q, kv, lane);
         for (int g = 0; g < p.G; ++g, ++it) {
           const int h = un.hkv * p.G + g;
           const int *sem = p.sem + (size_t)(un.b * p.H + h) * p.N + q;
           int ok = 1;
           if (lane == 0) {
-            ok = sem_wait(sem, rank, ab) ? 1 : 0;
-            if (ok) st_release_cta_shared(seen, it + 1);
+            if constexpr (L::kTurnRing) {
+              // the slot is free once the epilogue has released the step kTurns earlier
+              const uint32_t slot = it % kTurns, wrap = (it / kTurns) & 1;
+              ok = (mbar_wait(&bar.turn_empty[slot], wrap ^ 1, ab) && sem_wait(sem, rank, ab)) ? 1 : 0;
+              if (ok) mbar_arrive(&bar.turn_full[slot]);
+            } else {
+              ok = sem_wait(sem, rank, ab) ? 1 : 0;
+              if (ok) st_release_cta_shared(seen, it + 1);
+            }
           }
           if (!__shfl_sync(0xffffffffu, ok, 0)) return;
         }
@@ -590,7 +611,7 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
   }
 }
 
-template <int D, bool DET>
+template <int D, bool DET, int ODD>
 __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
                              const Abort &ab) {
   using L = BwdLayout<D, DET>;
@@ -614,14 +635,14 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w);
+    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg);
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg);
+      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg, ODD);
+      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD);
       for (int t = 0; ok && t < nsteps; ++t) {
         for (int g = 0; g < p.G; ++g, ++it) {
           const int h = un.hkv * p.G + g;
-          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t);
+          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t, ODD);
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
           int *sem = p.sem + tile_idx;
           if (!agree(et == 0 ? mbar_wait(bar.g5_done, it & 1, ab) : true)) {
@@ -665,7 +686,13 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           }
           // the semaphore counts the partials added so far: the contributor of rank r goes
           // once rank r-1 has released it; the poller warp has been watching it
-          if (DET && !agree(et == 0 ? counter_wait(seen, it + 1, ab) : true)) {
+          bool turn = true;
+          if constexpr (L::kTurnRing) {
+            if (et == 0) turn = mbar_wait(&bar.turn_full[it % kTurns], (it / kTurns) & 1, ab);
+          } else if constexpr (DET) {
+            if (et == 0) turn = counter_wait(seen, it + 1, ab);
+          }
+          if (DET && !agree(turn)) {
             ok = false;
             break;
           }
@@ -684,7 +711,10 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           }
           if (DET) {  // one release for the warpgroup, after all of its reductions
             named_bar_sync(1, 128);
-            if (et == 0) red_release_add(sem, 1);
+            if (et == 0) {
+              red_release_add(sem, 1);
+              if constexpr (L::kTurnRing) mbar_arrive(&bar.turn_empty[it % kTurns]);
+            }
           }
           if (et == 0) DASH_TRACE(p, 17);
         }
@@ -733,7 +763,7 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
 }
 
 // ---------------------------------------------------------------------------------------
-template <int D, bool DET>
+template <int D, bool DET, int ODD>
 __global__ void __launch_bounds__(512, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -767,6 +797,12 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar.dkv_full, 1);
     mbar_init(bar.dkv_empty, 4);
     mbar_init(bar.drain, 1);
+    if constexpr (L::kTurnRing) {
+      for (int i = 0; i < kTurns; ++i) {
+        mbar_init(&bar.turn_full[i], 1);
+        mbar_init(&bar.turn_empty[i], 1);
+      }
+    }
     *s_abort = 0;
     *reinterpret_cast<uint32_t *>(smem + L::offMisc + 16) = 0;  // semaphores acquired
     fence_mbar_init();
@@ -788,15 +824,15 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp < 4) {
     regs_set<RegSplit<D>::kCtl, RegSplit<D>::kLaunch>();
-    if (warp == 0) bwd_producer<D, DET>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
-    if (warp == 1) bwd_mma<D, DET>(p, smem, tmem, bar, ab);
-    if (DET && warp == 3) bwd_sem_poller<D, DET>(p, smem, ab);
+    if (warp == 0) bwd_producer<D, DET, ODD>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
+    if (warp == 1) bwd_mma<D, DET, ODD>(p, smem, tmem, bar, ab);
+    if (DET && warp == 3) bwd_sem_poller<D, DET, ODD>(p, smem, ab);
   } else if (warp < 12) {
     regs_set<RegSplit<D>::kSoftmax, RegSplit<D>::kLaunch>();
-    bwd_softmax_grad<D, DET>(p, smem, tmem, bar, ab);
+    bwd_softmax_grad<D, DET, ODD>(p, smem, tmem, bar, ab);
   } else {
     regs_set<RegSplit<D>::kEpi, RegSplit<D>::kLaunch>();
-    bwd_epilogue<D, DET>(p, smem, tmem, bar, ab);
+    bwd_epilogue<D, DET, ODD>(p, smem, tmem, bar, ab);
   }
 
   tc_fence_before();
@@ -807,11 +843,11 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int D, bool DET>
+template <int D, bool DET, int ODD>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &tdo, const BwdParams &p, int grid, cudaStream_t stream) {
   using L = BwdLayout<D, DET>;
-  auto kern = bwd_kernel<D, DET>;
+  auto kern = bwd_kernel<D, DET, ODD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   // the per-warpgroup register split assumes exactly 128 registers per thread at launch
@@ -825,14 +861,22 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 }  // namespace
 
-cudaError_t launch_bwd(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,
-                       const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, int grid,
-                       cudaStream_t stream) {
+template <int ODD>
+cudaError_t launch_bwd_o(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,
+                         const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, int grid,
+                         cudaStream_t stream) {
   if (D == 64)
-    return deterministic ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, grid, stream)
-                         : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, grid, stream);
-  return deterministic ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, grid, stream)
-                       : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, grid, stream);
+    return deterministic ? launch_bwd_t<64, true, ODD>(tq, tk, tv, tdo, p, grid, stream)
+                         : launch_bwd_t<64, false, ODD>(tq, tk, tv, tdo, p, grid, stream);
+  return deterministic ? launch_bwd_t<128, true, ODD>(tq, tk, tv, tdo, p, grid, stream)
+                       : launch_bwd_t<128, false, ODD>(tq, tk, tv, tdo, p, grid, stream);
+}
+
+cudaError_t launch_bwd(int D, bool deterministic, bool odd_sym_shift, const CUtensorMap &tq,
+                       const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
+                       const BwdParams &p, int grid, cudaStream_t stream) {
+  return odd_sym_shift ? launch_bwd_o<1>(D, deterministic, tq, tk, tv, tdo, p, grid, stream)
+                       : launch_bwd_o<0>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
 }
 
 }  // namespace dash

@@ -69,9 +69,11 @@ struct FwdParams {
 
 size_t fwd_smem_bytes(int D);
 
-cudaError_t launch_bwd(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,
-                       const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p,
-                       int grid, cudaStream_t stream);
+// odd_sym_shift: the launch runs Symmetric Shift (causal mask, shift traversal) with an odd
+// tile count, i.e. the padded schedule; the kernel is compiled for each case.
+cudaError_t launch_bwd(int D, bool deterministic, bool odd_sym_shift, const CUtensorMap &tq,
+                       const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
+                       const BwdParams &p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd(int D, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,

@@ -58,28 +58,32 @@ DASH_HD int traversal(int sched, int causal, int N) {
 }
 
 DASH_HD bool sym_shift(int sched, int causal) { return sched == kShift && causal; }
-// The padded tile count of Symmetric Shift (N rounded up to even) and its half.
-DASH_HD int sym_np(int N) { return N + (N & 1); }
-DASH_HD int sym_h(int N) { return (N + 1) >> 1; }
+// `odd` (below) is N & 1.  It only matters for Symmetric Shift; the backward kernel is
+// compiled once per value and receives it as a constant, so that an even N runs the plain
+// even-N arithmetic.  The padded tile count of Symmetric Shift (N rounded up to even) and
+// its half:
+DASH_HD int sym_np(int N, int odd) { return N + odd; }
+DASH_HD int sym_h(int N, int odd) { return (N + odd) >> 1; }
 
-DASH_HD int sched_workers(int sched, int causal, int N) {
-  return sym_shift(sched, causal) ? sym_h(N) : N;
+DASH_HD int sched_workers(int sched, int causal, int N, int odd) {
+  return sym_shift(sched, causal) ? sym_h(N, odd) : N;
 }
 // Segments of worker w: two for a Symmetric Shift pair, one for worker 0 of an odd N (its
 // partner would be the padding block).
-DASH_HD int sched_segments(int sched, int causal, int N, int w) {
+DASH_HD int sched_segments(int sched, int causal, int N, int w, int odd) {
+  (void)N;
   if (!sym_shift(sched, causal)) return 1;
-  return ((N & 1) && w == 0) ? 1 : 2;
+  return (odd && w == 0) ? 1 : 2;
 }
-DASH_HD int seg_kv(int sched, int causal, int N, int w, int seg) {
-  return (sym_shift(sched, causal) && seg == 1) ? sym_np(N) - 1 - w : w;
+DASH_HD int seg_kv(int sched, int causal, int N, int w, int seg, int odd) {
+  return (sym_shift(sched, causal) && seg == 1) ? sym_np(N, odd) - 1 - w : w;
 }
-DASH_HD int seg_steps(int sched, int causal, int N, int w, int seg) {
+DASH_HD int seg_steps(int sched, int causal, int N, int w, int seg, int odd) {
   if (!causal) return N;
-  if (sched == kShift) return seg == 0 ? N - w : w + 1 - (N & 1);
+  if (sched == kShift) return seg == 0 ? N - w : w + 1 - odd;
   return N - w;
 }
-DASH_HD int step_q(int sched, int causal, int N, int w, int seg, int t) {
+DASH_HD int step_q(int sched, int causal, int N, int w, int seg, int t, int odd) {
   switch (sched) {
     case kDescending:
       return N - 1 - t;
@@ -90,7 +94,7 @@ DASH_HD int step_q(int sched, int causal, int N, int w, int seg, int t) {
       }
       // t is the step among those kept; for odd N, skip the padded schedule's steps on
       // the padding tile (step h-1-w of segment 0, step 0 of segment 1)
-      const int odd = N & 1, Np = sym_np(N), h = sym_h(N);
+      const int Np = sym_np(N, odd), h = sym_h(N, odd);
       if (seg == 1) return Np - 1 - (t + odd);
       if (odd && t >= h - 1 - w) ++t;
       if (t < h) {
@@ -104,13 +108,13 @@ DASH_HD int step_q(int sched, int causal, int N, int w, int seg, int t) {
       return causal ? w + t : t;
   }
 }
-DASH_HD int dq_rank(int sched, int causal, int N, int q, int kv) {
+DASH_HD int dq_rank(int sched, int causal, int N, int q, int kv, int odd) {
   if (sched != kShift) return kv;
   if (!causal) {
     int r = q - kv;
     return r < 0 ? r + N : r;
   }
-  const int h = sym_h(N);
+  const int h = sym_h(N, odd);
   if (q < h) return q - kv;
   if (kv < h) {
     int r = q - h - kv;
@@ -129,20 +133,20 @@ DASH_HD int dq_rank(int sched, int causal, int N, int q, int kv) {
 // shift order above.
 
 // Worker (within its head) that owns KV block kv under the shift schedule.
-DASH_HD int shift_worker_of(int causal, int N, int kv) {
-  return (causal && kv >= sym_h(N)) ? sym_np(N) - 1 - kv : kv;
+DASH_HD int shift_worker_of(int causal, int N, int kv, int odd) {
+  return (causal && kv >= sym_h(N, odd)) ? sym_np(N, odd) - 1 - kv : kv;
 }
 // Step, within its worker's program, at which the shift worker owning block kv visits
 // query tile q; -1 if the tile is masked for that block (or kv is the padding block).
 // For the causal mask this is the step of the padded (even) schedule, whose order is the
 // accumulation order.
-DASH_HD int shift_visit_step(int causal, int N, int kv, int q) {
+DASH_HD int shift_visit_step(int causal, int N, int kv, int q, int odd) {
   if (!causal) {
     const int t = q - kv;
     return t < 0 ? t + N : t;
   }
   if (q < kv) return -1;
-  const int h = sym_h(N), Np = sym_np(N);
+  const int h = sym_h(N, odd), Np = sym_np(N, odd);
   if (kv < h) {  // worker c = kv, first segment
     if (q >= h) {
       const int t = q - h - kv;
@@ -163,32 +167,33 @@ DASH_HD void packed_phase(int W, int P, int hd, int w, int *lo, int *hi) {
 }
 // Contributions to tile q that precede (q, kv) and come from the phase's other workers
 // [c_begin, c_end) (a slice of the phase, so that the count can be split across threads).
-DASH_HD int packed_count_in_phase(int causal, int N, int q, int kv, int c_begin, int c_end) {
-  const int tme = shift_visit_step(causal, N, kv, q);
+DASH_HD int packed_count_in_phase(int causal, int N, int q, int kv, int c_begin, int c_end,
+                                  int odd) {
+  const int tme = shift_visit_step(causal, N, kv, q, odd);
   int n = 0;
   for (int c = c_begin; c < c_end; ++c) {
-    const int t1 = shift_visit_step(causal, N, c, q);
+    const int t1 = shift_visit_step(causal, N, c, q, odd);
     if (t1 >= 0 && t1 < tme) ++n;
     if (causal) {
-      const int t2 = shift_visit_step(causal, N, sym_np(N) - 1 - c, q);
+      const int t2 = shift_visit_step(causal, N, sym_np(N, odd) - 1 - c, q, odd);
       if (t2 >= 0 && t2 < tme) ++n;
     }
   }
   return n;
 }
 // Contributions to tile q from the workers [0, lo) of earlier rounds (all allowed blocks).
-DASH_HD int packed_count_before(int causal, int N, int q, int lo) {
+DASH_HD int packed_count_before(int causal, int N, int q, int lo, int odd) {
   if (!causal) return lo;
   const int a = lo < q + 1 ? lo : q + 1;             // blocks c <= q, c < lo
-  const int b = lo - (sym_np(N) - 1 - q);            // blocks Np-1-c <= q, c < lo
+  const int b = lo - (sym_np(N, odd) - 1 - q);       // blocks Np-1-c <= q, c < lo
   return a + (b > 0 ? b : 0);
 }
 // Rank of block kv in dQ tile q of head hd (full mask in closed form; the causal count is
 // the same definition evaluated over the phase's workers).
-DASH_HD int packed_rank(int causal, int N, int P, int hd, int q, int kv) {
-  const int W = causal ? sym_h(N) : N;
+DASH_HD int packed_rank(int causal, int N, int P, int hd, int q, int kv, int odd) {
+  const int W = causal ? sym_h(N, odd) : N;
   int lo, hi;
-  packed_phase(W, P, hd, shift_worker_of(causal, N, kv), &lo, &hi);
+  packed_phase(W, P, hd, shift_worker_of(causal, N, kv, odd), &lo, &hi);
   if (!causal) {
     const int Wp = hi - lo, k = kv - lo;
     int base = (q - lo) % N;
@@ -196,7 +201,8 @@ DASH_HD int packed_rank(int causal, int N, int P, int hd, int q, int kv) {
     const int in_phase = (base >= Wp - 1) ? Wp - 1 - k : (k <= base ? base - k : base + Wp - k);
     return lo + in_phase;
   }
-  return packed_count_before(causal, N, q, lo) + packed_count_in_phase(causal, N, q, kv, lo, hi);
+  return packed_count_before(causal, N, q, lo, odd) +
+         packed_count_in_phase(causal, N, q, kv, lo, hi, odd);
 }
 
 }  // namespace dash
