@@ -453,7 +453,6 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 pv[e] = ex2_approx(fmaf(__uint_as_float(sv[c + e]), p.scale_log2, -lv[e]));
-                if (diag && (c0 + c + e) < r) pv[e] = 0.f;
               }
               pk[c / 2] = pack_bf16(pv[0], pv[1]);
               pk[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
@@ -462,6 +461,18 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
           if (kv_pad) {  // uniform per thread: outside the exp loop
 #pragma unroll
             for (int m = 0; m < 32; ++m) pk[m] = 0u;
+          }
+          // causal diagonal tile: query column < key row r is masked.  Applied to the packed
+          // words once per diagonal step, not per element inside the exp loop (that loop is
+          // bound by instruction issue: a per-element select cost 9 % at D = 64); the
+          // unmasked exponentials computed there are overwritten here
+          if (diag) {
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {
+              const int col = c0 + 2 * m;
+              if (col + 1 < r) pk[m] = 0u;
+              else if (col < r) pk[m] &= 0xFFFF0000u;
+            }
           }
           // P^T (bf16x2) over the first 32 of this half's S^T columns, all read above: the
           // A operand of G3, which then runs while dS is computed
