@@ -298,8 +298,8 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
 #endif
   if ((stages & DASH_BWD_TILES) &&
       dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC,
-                       causal && (N & 1) && plan.sched == dash::kShift, tq, tk, tv, tdo, p,
-                       plan.grid, s) != cudaSuccess)
+                       causal ? (((N & 1) && plan.sched == dash::kShift) ? 2 : 1) : 0, tq, tk,
+                       tv, tdo, p, plan.grid, s) != cudaSuccess)
     return DASH_ERR_CUDA;
   if ((stages & DASH_BWD_EPILOGUE) &&
       dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, s) !=

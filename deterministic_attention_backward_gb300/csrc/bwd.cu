@@ -58,6 +58,11 @@
 namespace dash {
 namespace {
 
+// The tile kernel's compile-time mask mode (0 full, 1 causal, 2 causal with an odd tile
+// count under Symmetric Shift): whether the mask is causal, and the `odd` of the schedule.
+__host__ __device__ constexpr int causal_of(int mode) { return mode != 0 ? 1 : 0; }
+__host__ __device__ constexpr int odd_of(int mode) { return mode == 2 ? 1 : 0; }
+
 // Depth of the ring of mbarriers through which the semaphore poller hands a dQ tile's turn
 // to the epilogue (D = 128, ordered variant).
 constexpr int kTurns = 4;
@@ -176,7 +181,7 @@ struct Bars {
 
 // ---------------------------------------------------------------------------------------
 // TMA producer: the whole warp runs the loop; one elected lane issues the copies.
-template <int D, bool DET, int ODD>
+template <int D, bool DET, int MODE>
 __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                              const CUtensorMap *tdo, const BwdParams &p, uint8_t *smem,
                              const Bars<D, DET> &bar, const Abort &ab) {
@@ -190,10 +195,10 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
+    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg, ODD);
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD);
+      const int kv = seg_kv(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
+      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
       if (!mbar_wait_warp(bar.kv_empty, (seg_it & 1) ^ 1, ab)) {
         ok = false;
         break;
@@ -215,7 +220,7 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
       // GQA: the G query heads of a step are visited back to back, so every head keeps the
       // schedule's lock step
       for (int t = 0; ok && t < nsteps; ++t) {
-        const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t, ODD);
+        const int q = step_q(pl.sched, causal_of(MODE), p.N, un.w, seg, t, odd_of(MODE));
         for (int g = 0; g < p.G; ++g) {
           const int h = un.hkv * p.G + g;
           const int s = it % L::kStages;
@@ -259,7 +264,7 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
 // warp-uniform); one elected lane issues each tcgen05 instruction.  Once the
 // softmax-gradient warps have written P^T over the current S^T columns, G3 and then the
 // next step's S^T product are issued, so both run while those warps compute dS.
-template <int D, bool DET, int ODD>
+template <int D, bool DET, int MODE>
 __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
                         const Abort &ab) {
   using L = BwdLayout<D, DET>;
@@ -289,9 +294,9 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
+    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD) * p.G;
+      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE)) * p.G;
       // segment prologue: new K_j/V_j and G1 of the first step (the previous step's G3,
       // the last reader of the S^T columns, was issued before and runs first)
       if (!mbar_wait_warp(bar.kv_full, seg_it & 1, ab) ||
@@ -400,7 +405,7 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
 // columns just read (the A operand of G3); then, when dP^T has arrived, compute
 // dS^T = P^T (dP^T - Dvec) chunk by chunk and write it (bf16x2) back over the dP^T columns
 // just read; dS also goes to shared memory for G5.
-template <int D, bool DET, int ODD>
+template <int D, bool DET, int MODE>
 __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tmem,
                                  const Bars<D, DET> &bar, const Abort &ab) {
   using L = BwdLayout<D, DET>;
@@ -416,14 +421,14 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
+    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg, ODD);
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD);
+      const int kv = seg_kv(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
+      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
       for (int t = 0; ok && t < nsteps; ++t) {
         for (int g = 0; g < p.G; ++g, ++it) {
-          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t, ODD);
-          const bool diag = p.causal && (q == kv);
+          const int q = step_q(pl.sched, causal_of(MODE), p.N, un.w, seg, t, odd_of(MODE));
+          const bool diag = causal_of(MODE) && (q == kv);
           // a key row past S (partial last tile) reads zeros; its P is set to zero so that
           // nothing of it (not even an overflowing exp of -LSE) reaches dS
           const bool kv_pad = (p.S & (kTile - 1)) != 0 && kv * kTile + r >= p.S;
@@ -563,16 +568,16 @@ __device__ __forceinline__ UnitOrder unit_order(const BwdParams &p, const Plan &
   o.split = p.packed && (o.ph_hi - o.ph_lo) != pl.W;
   return o;
 }
-template <int ODD>
+template <int MODE>
 __device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, const UnitOrder &o,
                                          int q, int kv, int lane) {
-  if (!o.split) return dq_rank(pl.sched, p.causal, p.N, q, kv, ODD);
-  if (!p.causal) return packed_rank(0, p.N, (int)gridDim.x, o.hd, q, kv, 0);
+  if (!o.split) return dq_rank(pl.sched, causal_of(MODE), p.N, q, kv, odd_of(MODE));
+  if (!causal_of(MODE)) return packed_rank(0, p.N, (int)gridDim.x, o.hd, q, kv, 0);
   const int per = (o.ph_hi - o.ph_lo + 31) >> 5;
   const int cb = o.ph_lo + lane * per;
   const int ce = cb + per < o.ph_hi ? cb + per : o.ph_hi;
-  const int n = cb < ce ? packed_count_in_phase(1, p.N, q, kv, cb, ce, ODD) : 0;
-  return packed_count_before(1, p.N, q, o.ph_lo, ODD) + (int)__reduce_add_sync(0xffffffffu, n);
+  const int n = cb < ce ? packed_count_in_phase(1, p.N, q, kv, cb, ce, odd_of(MODE)) : 0;
+  return packed_count_before(1, p.N, q, o.ph_lo, odd_of(MODE)) + (int)__reduce_add_sync(0xffffffffu, n);
 }
 
 // Semaphore poller (warp 3, deterministic modes): walks this CTA's steps in the
@@ -582,7 +587,7 @@ __device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, con
 // number of steps acquired so far in shared memory (any number ahead; safe because a
 // tile's count only grows).  The L2 round trips of the polling thus overlap the
 // computation of the dQ partial instead of following its drain.
-template <int D, bool DET, int ODD>
+template <int D, bool DET, int MODE>
 __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &ab) {
   using L = BwdLayout<D, DET>;
   const int lane = lane_id();
@@ -593,13 +598,13 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
   for (int u = pl.first; u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
     const UnitOrder o = unit_order(p, pl, un);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
+    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
     for (int seg = 0; seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg, ODD);
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD);
+      const int kv = seg_kv(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
+      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
       for (int t = 0; t < nsteps; ++t) {
-        const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t, ODD);
-        const int rank = step_rank<ODD>(p, pl, o, q, kv, lane);
+        const int q = step_q(pl.sched, causal_of(MODE), p.N, un.w, seg, t, odd_of(MODE));
+        const int rank = step_rank<MODE>(p, pl, o, q, kv, lane);
         for (int g = 0; g < p.G; ++g, ++it) {
           const int h = un.hkv * p.G + g;
           const int *sem = p.sem + (size_t)(un.b * p.H + h) * p.N + q;
@@ -622,7 +627,7 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
   }
 }
 
-template <int D, bool DET, int ODD>
+template <int D, bool DET, int MODE>
 __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
                              const Abort &ab) {
   using L = BwdLayout<D, DET>;
@@ -646,14 +651,14 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, p.causal, p.N, un.w, ODD);
+    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, p.causal, p.N, un.w, seg, ODD);
-      const int nsteps = seg_steps(pl.sched, p.causal, p.N, un.w, seg, ODD);
+      const int kv = seg_kv(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
+      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
       for (int t = 0; ok && t < nsteps; ++t) {
         for (int g = 0; g < p.G; ++g, ++it) {
           const int h = un.hkv * p.G + g;
-          const int q = step_q(pl.sched, p.causal, p.N, un.w, seg, t, ODD);
+          const int q = step_q(pl.sched, causal_of(MODE), p.N, un.w, seg, t, odd_of(MODE));
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
           int *sem = p.sem + tile_idx;
           if (!agree(et == 0 ? mbar_wait(bar.g5_done, it & 1, ab) : true)) {
@@ -774,7 +779,7 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
 }
 
 // ---------------------------------------------------------------------------------------
-template <int D, bool DET, int ODD>
+template <int D, bool DET, int MODE>
 __global__ void __launch_bounds__(512, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -835,15 +840,15 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp < 4) {
     regs_set<RegSplit<D>::kCtl, RegSplit<D>::kLaunch>();
-    if (warp == 0) bwd_producer<D, DET, ODD>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
-    if (warp == 1) bwd_mma<D, DET, ODD>(p, smem, tmem, bar, ab);
-    if (DET && warp == 3) bwd_sem_poller<D, DET, ODD>(p, smem, ab);
+    if (warp == 0) bwd_producer<D, DET, MODE>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
+    if (warp == 1) bwd_mma<D, DET, MODE>(p, smem, tmem, bar, ab);
+    if (DET && warp == 3) bwd_sem_poller<D, DET, MODE>(p, smem, ab);
   } else if (warp < 12) {
     regs_set<RegSplit<D>::kSoftmax, RegSplit<D>::kLaunch>();
-    bwd_softmax_grad<D, DET, ODD>(p, smem, tmem, bar, ab);
+    bwd_softmax_grad<D, DET, MODE>(p, smem, tmem, bar, ab);
   } else {
     regs_set<RegSplit<D>::kEpi, RegSplit<D>::kLaunch>();
-    bwd_epilogue<D, DET, ODD>(p, smem, tmem, bar, ab);
+    bwd_epilogue<D, DET, MODE>(p, smem, tmem, bar, ab);
   }
 
   tc_fence_before();
@@ -854,11 +859,11 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int D, bool DET, int ODD>
+template <int D, bool DET, int MODE>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &tdo, const BwdParams &p, int grid, cudaStream_t stream) {
   using L = BwdLayout<D, DET>;
-  auto kern = bwd_kernel<D, DET, ODD>;
+  auto kern = bwd_kernel<D, DET, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   // the per-warpgroup register split assumes exactly 128 registers per thread at launch
@@ -872,22 +877,26 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 }  // namespace
 
-template <int ODD>
+// MODE: 0 full mask, 1 causal, 2 causal with the padded (odd-N) Symmetric Shift.  Inside
+// the kernel the mask and the parity are constants: the full-mask build carries no
+// diagonal or schedule branches of the causal one (measured: +2 % full mask).
+template <int MODE>
 cudaError_t launch_bwd_o(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, int grid,
                          cudaStream_t stream) {
   if (D == 64)
-    return deterministic ? launch_bwd_t<64, true, ODD>(tq, tk, tv, tdo, p, grid, stream)
-                         : launch_bwd_t<64, false, ODD>(tq, tk, tv, tdo, p, grid, stream);
-  return deterministic ? launch_bwd_t<128, true, ODD>(tq, tk, tv, tdo, p, grid, stream)
-                       : launch_bwd_t<128, false, ODD>(tq, tk, tv, tdo, p, grid, stream);
+    return deterministic ? launch_bwd_t<64, true, MODE>(tq, tk, tv, tdo, p, grid, stream)
+                         : launch_bwd_t<64, false, MODE>(tq, tk, tv, tdo, p, grid, stream);
+  return deterministic ? launch_bwd_t<128, true, MODE>(tq, tk, tv, tdo, p, grid, stream)
+                       : launch_bwd_t<128, false, MODE>(tq, tk, tv, tdo, p, grid, stream);
 }
 
-cudaError_t launch_bwd(int D, bool deterministic, bool odd_sym_shift, const CUtensorMap &tq,
+cudaError_t launch_bwd(int D, bool deterministic, int mode, const CUtensorMap &tq,
                        const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                        const BwdParams &p, int grid, cudaStream_t stream) {
-  return odd_sym_shift ? launch_bwd_o<1>(D, deterministic, tq, tk, tv, tdo, p, grid, stream)
-                       : launch_bwd_o<0>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+  if (mode == 2) return launch_bwd_o<2>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+  if (mode == 1) return launch_bwd_o<1>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+  return launch_bwd_o<0>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
 }
 
 }  // namespace dash

@@ -69,9 +69,10 @@ struct FwdParams {
 
 size_t fwd_smem_bytes(int D);
 
-// odd_sym_shift: the launch runs Symmetric Shift (causal mask, shift traversal) with an odd
-// tile count, i.e. the padded schedule; the kernel is compiled for each case.
-cudaError_t launch_bwd(int D, bool deterministic, bool odd_sym_shift, const CUtensorMap &tq,
+// mode: 0 = full mask; 1 = causal mask; 2 = causal mask under Symmetric Shift (shift
+// traversal) with an odd tile count, i.e. the padded schedule.  The tile kernel is compiled
+// once per mode, so the mask and the tile-count parity are constants inside it.
+cudaError_t launch_bwd(int D, bool deterministic, int mode, const CUtensorMap &tq,
                        const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                        const BwdParams &p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd(int D, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -59,8 +59,8 @@ DASH_HD int traversal(int sched, int causal, int N) {
 
 DASH_HD bool sym_shift(int sched, int causal) { return sched == kShift && causal; }
 // `odd` (below) is N & 1.  It only matters for Symmetric Shift; the backward kernel is
-// compiled once per value and receives it as a constant, so that an even N runs the plain
-// even-N arithmetic.  The padded tile count of Symmetric Shift (N rounded up to even) and
+// compiled per mask and parity and receives it (and `causal`) as constants, so that an
+// even N runs the plain even-N arithmetic.  The padded tile count of Symmetric Shift (N rounded up to even) and
 // its half:
 DASH_HD int sym_np(int N, int odd) { return N + odd; }
 DASH_HD int sym_h(int N, int odd) { return (N + odd) >> 1; }
