@@ -59,8 +59,7 @@ namespace dash {
 namespace {
 
 // The tile kernel's compile-time mask mode (0 full, 1 causal, 2 causal with an odd tile
-// count under Symmetric Shift): whether the mask is causal, and the `odd` of the schedule.
-__host__ __device__ constexpr int causal_of(int mode) { return mode != 0 ? 1 : 0; }
+// count under Symmetric Shift) and the `odd` of the schedule it implies.
 __host__ __device__ constexpr int odd_of(int mode) { return mode == 2 ? 1 : 0; }
 
 // Depth of the ring of mbarriers through which the semaphore poller hands a dQ tile's turn
@@ -127,6 +126,13 @@ constexpr int kRedPaceEvery = 4;
 constexpr uint32_t kRedPaceNs = 200;
 
 // Work of this CTA: worker u (head-major over all heads) runs on CTA (u mod grid), in order.
+// The mask of a launch: a constant in the full-mask build; read from the parameters in the
+// causal builds (measured: folding it there too cost 7 % on GQA shapes).
+template <int MODE>
+__device__ __forceinline__ int mode_causal(const BwdParams &p) {
+  return MODE == 0 ? 0 : p.causal;
+}
+
 struct Plan {
   int sched, W, first, stride, nunits, head_off;
 };
@@ -195,10 +201,10 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
+    const int nseg = sched_segments(pl.sched, mode_causal<MODE>(p), p.N, un.w, odd_of(MODE));
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
-      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
+      const int kv = seg_kv(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
+      const int nsteps = seg_steps(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
       if (!mbar_wait_warp(bar.kv_empty, (seg_it & 1) ^ 1, ab)) {
         ok = false;
         break;
@@ -220,7 +226,7 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
       // GQA: the G query heads of a step are visited back to back, so every head keeps the
       // schedule's lock step
       for (int t = 0; ok && t < nsteps; ++t) {
-        const int q = step_q(pl.sched, causal_of(MODE), p.N, un.w, seg, t, odd_of(MODE));
+        const int q = step_q(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, t, odd_of(MODE));
         for (int g = 0; g < p.G; ++g) {
           const int h = un.hkv * p.G + g;
           const int s = it % L::kStages;
@@ -294,9 +300,9 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
+    const int nseg = sched_segments(pl.sched, mode_causal<MODE>(p), p.N, un.w, odd_of(MODE));
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE)) * p.G;
+      const int nsteps = seg_steps(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE)) * p.G;
       // segment prologue: new K_j/V_j and G1 of the first step (the previous step's G3,
       // the last reader of the S^T columns, was issued before and runs first)
       if (!mbar_wait_warp(bar.kv_full, seg_it & 1, ab) ||
@@ -421,14 +427,14 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
+    const int nseg = sched_segments(pl.sched, mode_causal<MODE>(p), p.N, un.w, odd_of(MODE));
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
-      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
+      const int kv = seg_kv(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
+      const int nsteps = seg_steps(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
       for (int t = 0; ok && t < nsteps; ++t) {
         for (int g = 0; g < p.G; ++g, ++it) {
-          const int q = step_q(pl.sched, causal_of(MODE), p.N, un.w, seg, t, odd_of(MODE));
-          const bool diag = causal_of(MODE) && (q == kv);
+          const int q = step_q(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, t, odd_of(MODE));
+          const bool diag = mode_causal<MODE>(p) && (q == kv);
           // a key row past S (partial last tile) reads zeros; its P is set to zero so that
           // nothing of it (not even an overflowing exp of -LSE) reaches dS
           const bool kv_pad = (p.S & (kTile - 1)) != 0 && kv * kTile + r >= p.S;
@@ -571,8 +577,8 @@ __device__ __forceinline__ UnitOrder unit_order(const BwdParams &p, const Plan &
 template <int MODE>
 __device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, const UnitOrder &o,
                                          int q, int kv, int lane) {
-  if (!o.split) return dq_rank(pl.sched, causal_of(MODE), p.N, q, kv, odd_of(MODE));
-  if (!causal_of(MODE)) return packed_rank(0, p.N, (int)gridDim.x, o.hd, q, kv, 0);
+  if (!o.split) return dq_rank(pl.sched, mode_causal<MODE>(p), p.N, q, kv, odd_of(MODE));
+  if (!mode_causal<MODE>(p)) return packed_rank(0, p.N, (int)gridDim.x, o.hd, q, kv, 0);
   const int per = (o.ph_hi - o.ph_lo + 31) >> 5;
   const int cb = o.ph_lo + lane * per;
   const int ce = cb + per < o.ph_hi ? cb + per : o.ph_hi;
@@ -598,12 +604,12 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
   for (int u = pl.first; u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
     const UnitOrder o = unit_order(p, pl, un);
-    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
+    const int nseg = sched_segments(pl.sched, mode_causal<MODE>(p), p.N, un.w, odd_of(MODE));
     for (int seg = 0; seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
-      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
+      const int kv = seg_kv(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
+      const int nsteps = seg_steps(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
       for (int t = 0; t < nsteps; ++t) {
-        const int q = step_q(pl.sched, causal_of(MODE), p.N, un.w, seg, t, odd_of(MODE));
+        const int q = step_q(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, t, odd_of(MODE));
         const int rank = step_rank<MODE>(p, pl, o, q, kv, lane);
         for (int g = 0; g < p.G; ++g, ++it) {
           const int h = un.hkv * p.G + g;
@@ -651,14 +657,14 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
     const Unit un = decode_unit(p, pl, u);
-    const int nseg = sched_segments(pl.sched, causal_of(MODE), p.N, un.w, odd_of(MODE));
+    const int nseg = sched_segments(pl.sched, mode_causal<MODE>(p), p.N, un.w, odd_of(MODE));
     for (int seg = 0; ok && seg < nseg; ++seg) {
-      const int kv = seg_kv(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
-      const int nsteps = seg_steps(pl.sched, causal_of(MODE), p.N, un.w, seg, odd_of(MODE));
+      const int kv = seg_kv(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
+      const int nsteps = seg_steps(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
       for (int t = 0; ok && t < nsteps; ++t) {
         for (int g = 0; g < p.G; ++g, ++it) {
           const int h = un.hkv * p.G + g;
-          const int q = step_q(pl.sched, causal_of(MODE), p.N, un.w, seg, t, odd_of(MODE));
+          const int q = step_q(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, t, odd_of(MODE));
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
           int *sem = p.sem + tile_idx;
           if (!agree(et == 0 ? mbar_wait(bar.g5_done, it & 1, ab) : true)) {
@@ -877,9 +883,9 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 }  // namespace
 
-// MODE: 0 full mask, 1 causal, 2 causal with the padded (odd-N) Symmetric Shift.  Inside
-// the kernel the mask and the parity are constants: the full-mask build carries no
-// diagonal or schedule branches of the causal one (measured: +2 % full mask).
+// MODE: 0 full mask, 1 causal, 2 causal with the padded (odd-N) Symmetric Shift.  The
+// parity is a constant inside the kernel, and so is the mask in the full-mask build, which
+// then carries no diagonal or schedule branches of the causal one (measured: +2 %).
 template <int MODE>
 cudaError_t launch_bwd_o(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, int grid,

@@ -71,7 +71,7 @@ size_t fwd_smem_bytes(int D);
 
 // mode: 0 = full mask; 1 = causal mask; 2 = causal mask under Symmetric Shift (shift
 // traversal) with an odd tile count, i.e. the padded schedule.  The tile kernel is compiled
-// once per mode, so the mask and the tile-count parity are constants inside it.
+// once per mode.
 cudaError_t launch_bwd(int D, bool deterministic, int mode, const CUtensorMap &tq,
                        const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                        const BwdParams &p, int grid, cudaStream_t stream);
