@@ -22,9 +22,12 @@ def dash():
     return d
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("schedule", ["serial", "shift_fill"])
-def test_unreleased_semaphore_times_out_and_context_survives(dash, schedule):
-    B, S, H, D = 1, 512, 2, 64
+def test_unreleased_semaphore_times_out_and_context_survives(dash, schedule, D):
+    """D = 64 hands each turn to the epilogue through a shared-memory counter, D = 128
+    through a ring of mbarriers: both give up through the same abort flag."""
+    B, S, H = 1, 512, 2
     q, k, v, do = (t.cuda() for t in make_qkv_do(B, S, H, H, D, seed=0))
     o, lse = dash.fwd(q, k, v, causal=False, check=True)
     ws = torch.empty(dash.bwd_workspace_bytes(B, S, H, D), dtype=torch.uint8, device="cuda")
