@@ -87,8 +87,10 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           the mask and tile count (dash_sched_resolve names it): the pages
  *                           leave the choice to the user.  Measured over every configuration
  *                           of the benchmark (full and causal masks, D = 64 and 128,
- *                           S = 512 .. 16384, GQA 4:1), SHIFT_FILL is the fastest or within
- *                           1 % of it (odd tile counts included).  So AUTO = SHIFT_FILL. */
+ *                           S = 512 .. 16384, GQA 4:1, odd tile counts), SHIFT_FILL is the
+ *                           fastest or within 2 % of the fastest (SERIAL at S = 512, plain
+ *                           SHIFT on the GQA shape), and far ahead wherever the schedules
+ *                           differ.  So AUTO = SHIFT_FILL. */
 typedef enum {
   DASH_SCHED_ATOMIC = 0,
   DASH_SCHED_SERIAL = 1,
