@@ -19,8 +19,10 @@ import os
 import threading
 
 __all__ = ["fwd", "bwd", "bwd_workspace_bytes", "fwd_workspace_bytes", "status",
-           "sched_table", "sched_grid", "sched_resolve", "packed_rank", "fwd_varlen",
-           "bwd_varlen", "SCHEDULES", "lib", "DashError"]
+           "bwd_order_log", "set_wait_limit", "wait_limit", "sched_table", "sched_grid",
+           "sched_workers",
+           "sched_resolve", "packed_rank", "fwd_varlen", "bwd_varlen", "SCHEDULES", "lib",
+           "DashError"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdash_attn.so")
@@ -29,7 +31,9 @@ SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3, "shift_fill"
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "device-side wait timed out", 5: "workspace missing or too small"}
 EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_workspace_bytes",
-           "dash_attn_bwd", "dash_attn_bwd_stages", "dash_attn_status",
+           "dash_attn_bwd", "dash_attn_bwd_stages", "dash_attn_status", "dash_attn_bwd_status",
+           "dash_attn_set_wait_limit", "dash_attn_wait_limit", "dash_attn_bwd_order_log",
+           "dash_attn_noalloc_status",
            "dash_status_string", "dash_sched_workers", "dash_sched_segments", "dash_sched_steps",
            "dash_sched_step", "dash_sched_grid", "dash_sched_packed_rank", "dash_sched_resolve",
            "dash_attn_bwd_noalloc", "dash_attn_bwd_varlen_workspace_bytes",
@@ -82,6 +86,17 @@ def lib() -> ctypes.CDLL:
         L.dash_attn_bwd_varlen.restype = i
         L.dash_attn_status.argtypes = [vp, vp]
         L.dash_attn_status.restype = i
+        L.dash_attn_bwd_status.argtypes = [vp, vp]
+        L.dash_attn_bwd_status.restype = i
+        L.dash_attn_noalloc_status.argtypes = [vp]
+        L.dash_attn_noalloc_status.restype = i
+        L.dash_attn_set_wait_limit.argtypes = [ctypes.c_double]
+        L.dash_attn_set_wait_limit.restype = i
+        L.dash_attn_wait_limit.argtypes = []
+        L.dash_attn_wait_limit.restype = ctypes.c_double
+        L.dash_attn_bwd_order_log.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                              f, i, i, vp, sz, vp, vp]
+        L.dash_attn_bwd_order_log.restype = i
         L.dash_status_string.argtypes = [i]
         L.dash_status_string.restype = ctypes.c_char_p
         L.dash_sched_workers.argtypes = [i, i, i]
@@ -208,7 +223,42 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, schedule: str = "shift",
 def status(workspace, stream=None):
     """Synchronise and raise DashError if the last call on ``workspace`` reported a
     device-side failure (a bounded wait that ran out)."""
-    _check(lib().dash_attn_status(workspace.data_ptr(), _stream_ptr(stream)), "device status")
+    _check(lib().dash_attn_bwd_status(workspace.data_ptr(), _stream_ptr(stream)), "device status")
+
+
+def bwd_order_log(q, k, v, o, do, lse, causal: bool = False, schedule: str = "shift",
+                  scale: float | None = None, stream=None):
+    """Backward through ``dash_attn_bwd_order_log``: returns (dQ, dK, dV, order) where
+    order [B, H, N, N] int32 holds, for each visited (q tile, kv block), the rank at which
+    the block's dQ partial was added into the tile (-1 where the schedule skips the pair)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _require(t, n, torch.bfloat16)
+    _require(lse, "lse", torch.float32)
+    B, S, H, Hkv, D = _dims(q, k)
+    N = (S + 127) // 128
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    order = torch.full((B, H, N, N), -1, dtype=torch.int32, device=q.device)
+    ws = _workspace(bwd_workspace_bytes(B, S, H, D) or 256, q.device)
+    code = lib().dash_attn_bwd_order_log(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                                         dk.data_ptr(), dv.data_ptr(), B, S, H, H // Hkv, D,
+                                         float(scale) if scale else 0.0, int(bool(causal)),
+                                         SCHEDULES[schedule], ws.data_ptr(),
+                                         ws.numel() * ws.element_size(), order.data_ptr(),
+                                         _stream_ptr(stream))
+    _check(code, "dash_attn_bwd_order_log")
+    status(ws, stream)
+    return dq, dk, dv, order
+
+
+def set_wait_limit(seconds: float):
+    """Limit of one device-side bounded wait for later calls (process-wide)."""
+    _check(lib().dash_attn_set_wait_limit(float(seconds)), "dash_attn_set_wait_limit")
+
+
+def wait_limit() -> float:
+    return float(lib().dash_attn_wait_limit())
 
 
 def sched_resolve(schedule: str, causal: bool, N: int) -> str:
@@ -217,6 +267,14 @@ def sched_resolve(schedule: str, causal: bool, N: int) -> str:
     if r < 0:
         raise ValueError("unsupported schedule arguments")
     return {v: k for k, v in SCHEDULES.items()}[r]
+
+
+def sched_workers(schedule: str, causal: bool, N: int) -> int:
+    """Workers per head of ``schedule`` at N tiles."""
+    w = lib().dash_sched_workers(SCHEDULES[schedule], int(bool(causal)), N)
+    if w < 0:
+        raise ValueError("unsupported schedule arguments")
+    return w
 
 
 def sched_grid(schedule: str, causal: bool, N: int, heads: int, sms: int) -> int:

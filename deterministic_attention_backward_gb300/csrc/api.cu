@@ -3,6 +3,7 @@
 // sequence of the forward and backward passes.  No device memory is allocated here.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -97,26 +98,33 @@ struct BwdWorkspace {
   size_t dqacc_bytes, sem_bytes, total;
 };
 
-// Row arrays are per tile: S padded up to N*128 rows per (b, h).
+// [status 256 B][semaphores][lse2][Dvec][dQ accumulator], each part 256-byte aligned; the
+// status block and the semaphores are contiguous so that one clear covers both.  Row arrays
+// are per tile: S padded up to N*128 rows per (b, h).
 BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
   BwdWorkspace w{};
-  const size_t rows = (size_t)B * H * tiles(S) * kTile;
+  const size_t ntiles = (size_t)B * H * tiles(S);
+  const size_t rows = ntiles * kTile;
+  char *base = static_cast<char *>(ws);
   size_t off = 0;
-  w.status = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + off);
+  w.status = reinterpret_cast<uint32_t *>(base + off);
   off += kStatusBytes;
-  w.dqacc = reinterpret_cast<float *>(static_cast<char *>(ws) + off);
+  w.sem = reinterpret_cast<int *>(base + off);
+  w.sem_bytes = ntiles * 4;
+  off = align256(off + w.sem_bytes);
+  w.lse2 = reinterpret_cast<float *>(base + off);
+  off = align256(off + rows * 4);
+  w.dvec = reinterpret_cast<float *>(base + off);
+  off = align256(off + rows * 4);
+  w.dqacc = reinterpret_cast<float *>(base + off);
   w.dqacc_bytes = rows * D * 4;
   off = align256(off + w.dqacc_bytes);
-  w.lse2 = reinterpret_cast<float *>(static_cast<char *>(ws) + off);
-  off = align256(off + rows * 4);
-  w.dvec = reinterpret_cast<float *>(static_cast<char *>(ws) + off);
-  off = align256(off + rows * 4);
-  w.sem = reinterpret_cast<int *>(static_cast<char *>(ws) + off);
-  w.sem_bytes = (size_t)B * H * tiles(S) * 4;
-  off = align256(off + w.sem_bytes);
   w.total = off;
   return w;
 }
+
+// Limit of one bounded wait inside the kernels (dash_attn_set_wait_limit).
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
 
 #ifdef DASH_TRACE_BUILD
 unsigned long long *g_trace = nullptr;  // development trace build only
@@ -129,6 +137,8 @@ struct LaunchPlan {
   int sched, workers, grid, packed;
 };
 
+bool sched_known(int sched) { return sched >= DASH_SCHED_ATOMIC && sched <= DASH_SCHED_AUTO; }
+
 // DASH_SCHED_AUTO: SHIFT_FILL (the measured choice for every mask, head dim and length;
 // see the header).
 int resolve_sched(int sched, int mask, int N) {
@@ -137,9 +147,9 @@ int resolve_sched(int sched, int mask, int N) {
   return sched == DASH_SCHED_AUTO ? DASH_SCHED_SHIFT_FILL : sched;
 }
 
-// False when plain SHIFT cannot have every worker of a head resident at once.  SHIFT_FILL
-// has no such limit: its ranks follow the time order of the rounds, so a head wider than
-// the grid simply spans more rounds.
+// False when plain SHIFT cannot have every worker of a head resident at once.  The packed
+// schedules have no such limit: their ranks follow the time order of the rounds, so a head
+// wider than the grid simply spans more rounds.
 bool make_plan(int sched, int causal, int N, int heads, int sms, LaunchPlan *pl) {
   pl->sched = dash::traversal(sched, causal, N);
   pl->workers = dash::sched_workers(pl->sched, causal, N, N & 1);
@@ -203,6 +213,7 @@ static dash_status_t fwd_impl(const void *q, const void *k, const void *v, void 
   p.N = tiles(S);
   p.causal = mask == DASH_MASK_CAUSAL;
   p.scale_log2 = resolve_scale(scale, D) * dash::kLog2e;
+  p.wait_ns = g_wait_ns.load();
   return dash::launch_fwd(D, tq, tk, tv, p, s) == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
@@ -219,17 +230,18 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
                               int B, int S, int H, int group, int D, float scale,
                               dash_mask_t mask, dash_sched_t sched, void *workspace,
                               size_t workspace_bytes, unsigned stages, dash_stream_t stream,
-                              bool keep_status) {
+                              bool keep_status, int *order_log) {
   if (stages == 0 || (stages & ~unsigned(DASH_BWD_ALL))) return DASH_ERR_INVALID;
   dash_status_t st = check_sizes(B, S, H, group, D);
   if (st != DASH_OK) return st;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
-  if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_AUTO) return DASH_ERR_INVALID;
+  if (!sched_known(sched)) return DASH_ERR_INVALID;
   sched = (dash_sched_t)resolve_sched(sched, mask, tiles(S));
   const void *ptrs[] = {q, k, v, o, dout, dq, dk, dv};
   for (const void *ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return DASH_ERR_INVALID;
   if (!lse || !aligned4(lse)) return DASH_ERR_INVALID;
+  if (order_log && !aligned4(order_log)) return DASH_ERR_INVALID;
   const int N = tiles(S);
   const int causal = mask == DASH_MASK_CAUSAL;
   const BwdWorkspace need = carve_bwd(nullptr, B, S, H, D);
@@ -241,6 +253,7 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   LaunchPlan plan;
   // every worker of a head must be resident at once for the shift schedules
   if (!make_plan(sched, causal, N, B * Hkv, dev.sms, &plan)) return DASH_ERR_UNSUPPORTED;
+  const bool ordered = sched != DASH_SCHED_ATOMIC;
 
   CUtensorMap tq, tk, tv, tdo;
   if (!make_bshd_map(&tq, q, B, S, H, D) || !make_bshd_map(&tk, k, B, S, Hkv, D) ||
@@ -251,15 +264,14 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   const BwdWorkspace w = carve_bwd(workspace, B, S, H, D);
   const float sc = resolve_scale(scale, D);
   if (stages & DASH_BWD_PROLOGUE) {
-    // status word + dQ accumulator are contiguous; semaphores separately
-    if ((keep_status ? cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes, s)
-                     : cudaMemsetAsync(w.status, 0, kStatusBytes + w.dqacc_bytes, s)) !=
-            cudaSuccess ||
-        cudaMemsetAsync(w.sem, 0, w.sem_bytes, s) != cudaSuccess)
+    // status word and semaphores are contiguous; the accumulator separately
+    if ((keep_status ? cudaMemsetAsync(w.sem, 0, w.sem_bytes, s)
+                     : cudaMemsetAsync(w.status, 0, kStatusBytes + w.sem_bytes, s)) != cudaSuccess ||
+        cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes, s) != cudaSuccess)
       return DASH_ERR_CUDA;
     // a partial last tile: its padding rows of lse2 / Dvec must read as zero
     if ((S % kTile) &&
-        cudaMemsetAsync(w.lse2, 0, reinterpret_cast<char *>(w.sem) - reinterpret_cast<char *>(w.lse2),
+        cudaMemsetAsync(w.lse2, 0, reinterpret_cast<char *>(w.dqacc) - reinterpret_cast<char *>(w.lse2),
                         s) != cudaSuccess)
       return DASH_ERR_CUDA;
     if (dash::launch_preprocess(static_cast<const __nv_bfloat16 *>(o),
@@ -276,6 +288,7 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   p.status = w.status;
   p.dk = static_cast<__nv_bfloat16 *>(dk);
   p.dv = static_cast<__nv_bfloat16 *>(dv);
+  p.order_log = ordered ? order_log : nullptr;
   p.B = B;
   p.S = S;
   p.H = H;
@@ -287,6 +300,7 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   p.sched = plan.sched;
   p.workers = plan.workers;
   p.packed = plan.packed;
+  p.wait_ns = g_wait_ns.load();
   p.scale_log2 = sc * dash::kLog2e;
   p.scale = sc;
 #ifdef DASH_TRACE_BUILD
@@ -297,9 +311,8 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   p.trace_cta = 0;
 #endif
   if ((stages & DASH_BWD_TILES) &&
-      dash::launch_bwd(D, sched != DASH_SCHED_ATOMIC,
-                       causal ? (((N & 1) && plan.sched == dash::kShift) ? 2 : 1) : 0, tq, tk,
-                       tv, tdo, p, plan.grid, s) != cudaSuccess)
+      dash::launch_bwd(D, ordered, causal ? (((N & 1) && plan.sched == dash::kShift) ? 2 : 1) : 0,
+                       tq, tk, tv, tdo, p, plan.grid, s) != cudaSuccess)
     return DASH_ERR_CUDA;
   if ((stages & DASH_BWD_EPILOGUE) &&
       dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, s) !=
@@ -315,8 +328,28 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
                                    size_t workspace_bytes, unsigned stages,
                                    dash_stream_t stream) {
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, S, H, group, D, scale, mask, sched,
-                  workspace, workspace_bytes, stages, stream, false);
+                  workspace, workspace_bytes, stages, stream, false, nullptr);
 }
+
+dash_status_t dash_attn_bwd_order_log(const void *q, const void *k, const void *v,
+                                      const void *o, const void *dout, const float *lse,
+                                      void *dq, void *dk, void *dv, int B, int S, int H,
+                                      int group, int D, float scale, dash_mask_t mask,
+                                      dash_sched_t sched, void *workspace,
+                                      size_t workspace_bytes, int *order_log,
+                                      dash_stream_t stream) {
+  if (!order_log) return DASH_ERR_INVALID;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, S, H, group, D, scale, mask, sched,
+                  workspace, workspace_bytes, DASH_BWD_ALL, stream, false, order_log);
+}
+
+dash_status_t dash_attn_set_wait_limit(double seconds) {
+  if (!(seconds >= 1e-3 && seconds <= 3600.0)) return DASH_ERR_INVALID;
+  g_wait_ns.store((unsigned long long)(seconds * 1e9));
+  return DASH_OK;
+}
+
+double dash_attn_wait_limit(void) { return (double)g_wait_ns.load() * 1e-9; }
 
 dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o,
                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
@@ -383,7 +416,7 @@ dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, 
   if (st != DASH_OK) return st;
   if (H <= 0 || group <= 0 || H % group) return DASH_ERR_INVALID;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
-  if (sched < DASH_SCHED_ATOMIC || sched > DASH_SCHED_AUTO) return DASH_ERR_INVALID;
+  if (!sched_known(sched)) return DASH_ERR_INVALID;
   // refuse before enqueuing anything: every sequence must be runnable with this schedule
   DevInfo dev;
   if ((st = device_info(&dev)) != DASH_OK) return st;
@@ -410,7 +443,7 @@ dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, 
                   static_cast<const __nv_bfloat16 *>(dout) + qo, lse + (size_t)s0 * H,
                   static_cast<__nv_bfloat16 *>(dq) + qo, static_cast<__nv_bfloat16 *>(dk) + ko,
                   static_cast<__nv_bfloat16 *>(dv) + ko, 1, S, H, group, D, scale, mask, sched,
-                  workspace, workspace_bytes, DASH_BWD_ALL, stream, !first);
+                  workspace, workspace_bytes, DASH_BWD_ALL, stream, !first, nullptr);
     if (st != DASH_OK) return st;
     first = false;
   }
@@ -428,6 +461,10 @@ dash_status_t dash_attn_status(void *workspace, dash_stream_t stream) {
     return DASH_ERR_TIMEOUT;
   if (word) return DASH_ERR_CUDA;
   return DASH_OK;
+}
+
+dash_status_t dash_attn_bwd_status(void *workspace, dash_stream_t stream) {
+  return dash_attn_status(workspace, stream);
 }
 
 const char *dash_status_string(dash_status_t s) {
@@ -459,7 +496,7 @@ void dash_debug_set_trace(unsigned long long *buf, int cta) {
 
 // ------------------------------------------------------------------ schedule queries
 static bool sched_args_ok(int &sched, int mask, int N) {
-  if (sched < 0 || sched > DASH_SCHED_AUTO || (mask != 0 && mask != 1) || N <= 0) return false;
+  if (!sched_known(sched) || (mask != 0 && mask != 1) || N <= 0) return false;
   sched = resolve_sched(sched, mask, N);
   return true;
 }

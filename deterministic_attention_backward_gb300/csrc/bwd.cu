@@ -559,8 +559,8 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
 // ---------------------------------------------------------------------------------------
 // The dQ-tile order of one worker: the rank of its contribution to query tile q from KV
 // block kv.  Plain shift order when the head's workers share one round of the grid, else
-// the packed-shift count (full mask in closed form; causal: the phase's earlier
-// contributions, counted a slice per lane, so all 32 lanes of the warp must call it).
+// the packed-shift rank within the worker's phase (closed forms, sched.cuh), the phase being
+// fixed for the whole unit.
 struct UnitOrder {
   int ph_lo, ph_hi, hd;
   bool split;
@@ -576,14 +576,9 @@ __device__ __forceinline__ UnitOrder unit_order(const BwdParams &p, const Plan &
 }
 template <int MODE>
 __device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, const UnitOrder &o,
-                                         int q, int kv, int lane) {
+                                         int q, int kv) {
   if (!o.split) return dq_rank(pl.sched, mode_causal<MODE>(p), p.N, q, kv, odd_of(MODE));
-  if (!mode_causal<MODE>(p)) return packed_rank(0, p.N, (int)gridDim.x, o.hd, q, kv, 0);
-  const int per = (o.ph_hi - o.ph_lo + 31) >> 5;
-  const int cb = o.ph_lo + lane * per;
-  const int ce = cb + per < o.ph_hi ? cb + per : o.ph_hi;
-  const int n = cb < ce ? packed_count_in_phase(1, p.N, q, kv, cb, ce, odd_of(MODE)) : 0;
-  return packed_count_before(1, p.N, q, o.ph_lo, odd_of(MODE)) + (int)__reduce_add_sync(0xffffffffu, n);
+  return rank_in_phase(mode_causal<MODE>(p), p.N, q, kv, o.ph_lo, o.ph_hi, odd_of(MODE));
 }
 
 // Semaphore poller (warp 3, deterministic modes): walks this CTA's steps in the
@@ -610,7 +605,7 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
       const int nsteps = seg_steps(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
       for (int t = 0; t < nsteps; ++t) {
         const int q = step_q(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, t, odd_of(MODE));
-        const int rank = step_rank<MODE>(p, pl, o, q, kv, lane);
+        const int rank = step_rank<MODE>(p, pl, o, q, kv);
         for (int g = 0; g < p.G; ++g, ++it) {
           const int h = un.hkv * p.G + g;
           const int *sem = p.sem + (size_t)(un.b * p.H + h) * p.N + q;
@@ -625,6 +620,8 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
               ok = sem_wait(sem, rank, ab) ? 1 : 0;
               if (ok) st_release_cta_shared(seen, it + 1);
             }
+            // audit record of the executed order (dash_attn_bwd_order_log)
+            if (ok && p.order_log) p.order_log[(size_t)(sem - p.sem) * p.N + kv] = rank;
           }
           if (!__shfl_sync(0xffffffffu, ok, 0)) return;
         }
@@ -799,7 +796,7 @@ __global__ void __launch_bounds__(512, 1)
   const Bars<D, DET> bar(smem);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L::offMisc);
   int *s_abort = reinterpret_cast<int *>(smem + L::offMisc + 4);
-  const Abort ab{s_abort, p.status};
+  const Abort ab{s_abort, p.status, p.wait_ns};
   const int warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
@@ -848,7 +845,9 @@ __global__ void __launch_bounds__(512, 1)
     regs_set<RegSplit<D>::kCtl, RegSplit<D>::kLaunch>();
     if (warp == 0) bwd_producer<D, DET, MODE>(&tm_q, &tm_k, &tm_v, &tm_do, p, smem, bar, ab);
     if (warp == 1) bwd_mma<D, DET, MODE>(p, smem, tmem, bar, ab);
-    if (DET && warp == 3) bwd_sem_poller<D, DET, MODE>(p, smem, ab);
+    if constexpr (DET) {
+      if (warp == 3) bwd_sem_poller<D, DET, MODE>(p, smem, ab);
+    }
   } else if (warp < 12) {
     regs_set<RegSplit<D>::kSoftmax, RegSplit<D>::kLaunch>();
     bwd_softmax_grad<D, DET, MODE>(p, smem, tmem, bar, ab);
@@ -877,7 +876,20 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != (int)RegSplit<D>::kLaunch) return cudaErrorInvalidConfiguration;
-  kern<<<grid, 512, L::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  // ordered schedules: workers wait on workers of other CTAs, so every CTA must be resident
+  // at once; a cooperative launch makes the runtime guarantee that (or refuse the launch)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(512);
+  cfg.dynamicSmemBytes = L::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = DET ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

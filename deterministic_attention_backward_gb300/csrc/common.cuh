@@ -24,19 +24,21 @@ enum : uint32_t {
 
 // Backward kernel parameters (besides the TMA descriptors of Q, K, V, dO).
 struct BwdParams {
-  const float *lse2;  // [B,H,S]  LSE * log2(e)
-  const float *dvec;  // [B,H,S]  rowsum(dO * O)
+  const float *lse2;  // [B,H,N*128]  LSE * log2(e)
+  const float *dvec;  // [B,H,N*128]  rowsum(dO * O)
   float *dqacc;       // fp32 dQ accumulator, tile-native layout [B,H,N][D/4][128][4]
   int *sem;           // [B,H,N] dQ ordering semaphores (number of partials added so far)
   uint32_t *status;   // status word (error bit flags)
   __nv_bfloat16 *dk;  // [B,S,Hkv,D]
   __nv_bfloat16 *dv;  // [B,S,Hkv,D]
+  int *order_log;     // optional [B,H,N,N]: rank of (q, kv) in tile q's order, as executed
   int B, S, H, Hkv, G, N;
   int causal;
   int heads;    // B * Hkv (b, kv head) pairs
   int sched;    // visiting order of the workers (sched.cuh)
   int workers;  // workers per head
   int packed;   // dQ ranks of the packed shift (workers dealt round-robin over the grid)
+  unsigned long long wait_ns;  // limit of one bounded wait
   float scale_log2; // scale * log2(e)
   float scale;
   unsigned long long *trace;  // development trace build only: [64 steps][32 events] clock64
@@ -62,6 +64,7 @@ struct FwdParams {
   __nv_bfloat16 *o;  // [B,S,H,D]
   float *lse;        // [B,H,S]
   uint32_t *status;
+  unsigned long long wait_ns;  // limit of one bounded wait
   int B, S, H, Hkv, G, N;
   int causal;
   float scale_log2;
@@ -72,6 +75,8 @@ size_t fwd_smem_bytes(int D);
 // mode: 0 = full mask; 1 = causal mask; 2 = causal mask under Symmetric Shift (shift
 // traversal) with an odd tile count, i.e. the padded schedule.  The tile kernel is compiled
 // once per mode.
+// The ordered (deterministic) launch is cooperative: the runtime starts it only with every
+// CTA of the grid resident at once, so a worker never waits on a CTA that cannot start.
 cudaError_t launch_bwd(int D, bool deterministic, int mode, const CUtensorMap &tq,
                        const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                        const BwdParams &p, int grid, cudaStream_t stream);

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256, 1)
   const FBars<D> bar(smem);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L::offMisc);
   int *s_abort = reinterpret_cast<int *>(smem + L::offMisc + 4);
-  const Abort ab{s_abort, p.status};
+  const Abort ab{s_abort, p.status, p.wait_ns};
   const int warp = warp_id(), lane = lane_id();
 
   // heaviest causal tiles first

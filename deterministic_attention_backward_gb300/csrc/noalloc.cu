@@ -62,3 +62,12 @@ extern "C" dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, con
   return dash_attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, S, H, group, D, scale, mask, sched,
                        scratch, (size_t)DASH_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+// The status word sits at the start of the array, where dash_attn_bwd keeps it in any
+// workspace.
+extern "C" dash_status_t dash_attn_noalloc_status(dash_stream_t stream) {
+  void *scratch = nullptr;
+  const dash_status_t st = scratch_address(&scratch);
+  if (st != DASH_OK) return st;
+  return dash_attn_status(scratch, stream);
+}

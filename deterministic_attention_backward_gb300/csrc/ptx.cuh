@@ -12,6 +12,7 @@
 
 namespace dash {
 
+// Default limit of one bounded wait (the host may pass another through the parameters).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -32,6 +33,7 @@ __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 struct Abort {
   volatile int *cta;          // shared memory
   volatile uint32_t *global;  // workspace status word
+  uint64_t limit_ns;          // how long one wait may last before it gives up
   __device__ __forceinline__ bool set() const { return *cta != 0; }
   __device__ __forceinline__ void raise(uint32_t code) const {
     *cta = 1;
@@ -84,7 +86,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     if (ab.set()) return false;
     if ((it & 255u) == 0) {
       if (ab.poll_global()) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
+      if (globaltimer() - t0 > ab.limit_ns) {
         ab.raise(kErrMbarTimeout);
         return false;
       }
@@ -108,7 +110,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, c
         } else if ((it & 255u) == 255u) {
           if (ab.poll_global()) {
             stop = 1;
-          } else if (globaltimer() - t0 > kWaitTimeoutNs) {
+          } else if (globaltimer() - t0 > ab.limit_ns) {
             ab.raise(kErrMbarTimeout);
             stop = 1;
           }
@@ -437,7 +439,7 @@ __device__ __forceinline__ bool sem_wait(const int *sem, int want, const Abort &
     if (ab.set()) return false;
     if ((it & 63u) == 0) {
       if (ab.poll_global()) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
+      if (globaltimer() - t0 > ab.limit_ns) {
         ab.raise(kErrSemTimeout);
         return false;
       }
@@ -465,7 +467,7 @@ __device__ __forceinline__ bool counter_wait(const uint32_t *ctr, uint32_t want,
     if (ab.set()) return false;
     if ((it & 63u) == 0) {
       if (ab.poll_global()) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
+      if (globaltimer() - t0 > ab.limit_ns) {
         ab.raise(kErrSemTimeout);
         return false;
       }

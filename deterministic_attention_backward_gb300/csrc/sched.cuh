@@ -165,22 +165,6 @@ DASH_HD void packed_phase(int W, int P, int hd, int w, int *lo, int *hi) {
   *lo = (int)(a < 0 ? 0 : a);
   *hi = (int)(b > W ? W : b);
 }
-// Contributions to tile q that precede (q, kv) and come from the phase's other workers
-// [c_begin, c_end) (a slice of the phase, so that the count can be split across threads).
-DASH_HD int packed_count_in_phase(int causal, int N, int q, int kv, int c_begin, int c_end,
-                                  int odd) {
-  const int tme = shift_visit_step(causal, N, kv, q, odd);
-  int n = 0;
-  for (int c = c_begin; c < c_end; ++c) {
-    const int t1 = shift_visit_step(causal, N, c, q, odd);
-    if (t1 >= 0 && t1 < tme) ++n;
-    if (causal) {
-      const int t2 = shift_visit_step(causal, N, sym_np(N, odd) - 1 - c, q, odd);
-      if (t2 >= 0 && t2 < tme) ++n;
-    }
-  }
-  return n;
-}
 // Contributions to tile q from the workers [0, lo) of earlier rounds (all allowed blocks).
 DASH_HD int packed_count_before(int causal, int N, int q, int lo, int odd) {
   if (!causal) return lo;
@@ -188,21 +172,53 @@ DASH_HD int packed_count_before(int causal, int N, int q, int lo, int odd) {
   const int b = lo - (sym_np(N, odd) - 1 - q);       // blocks Np-1-c <= q, c < lo
   return a + (b > 0 ? b : 0);
 }
-// Rank of block kv in dQ tile q of head hd (full mask in closed form; the causal count is
-// the same definition evaluated over the phase's workers).
-DASH_HD int packed_rank(int causal, int N, int P, int hd, int q, int kv, int odd) {
-  const int W = causal ? sym_h(N, odd) : N;
-  int lo, hi;
-  packed_phase(W, P, hd, shift_worker_of(causal, N, kv, odd), &lo, &hi);
+DASH_HD int span(int lo, int hi) { return hi > lo ? hi - lo : 0; }
+DASH_HD int imax(int a, int b) { return a > b ? a : b; }
+DASH_HD int imin(int a, int b) { return a < b ? a : b; }
+// Contributions to tile q that precede (q, kv) in time and come from the workers c in
+// [a, b) of kv's phase (all c < h), causal mask.  The Symmetric Shift visit steps of tile q
+// by worker c are, per block,
+//   block c, q >= h:      (q - h - c) mod h   = d - c (c <= d) or d - c + h (c > d), d = q - h
+//   block c, q <  h:      h + q - c           (c <= q)
+//   block Np-1-c:         (Np - c) + (Np-1-q) (c >= Np-1-q)
+// and each is below tme on one contiguous range of c, so the count is a sum of range
+// lengths.  Equal to the loop above (tested against the oracle's lock-step simulation).
+DASH_HD int causal_count_in_phase(int N, int q, int kv, int a, int b, int odd) {
+  const int tme = shift_visit_step(1, N, kv, q, odd);
+  const int h = sym_h(N, odd), Np = sym_np(N, odd);
+  const int bb = imin(b, h);
+  int n;
+  if (q >= h) {
+    const int d = q - h;
+    n = span(imax(imax(a, d - tme + 1), 0), imin(bb, d + 1)) +
+        span(imax(imax(a, d + 1), d + h - tme + 1), bb);
+  } else {
+    n = span(imax(imax(a, h + q - tme + 1), 0), imin(bb, q + 1));
+  }
+  return n + span(imax(imax(a, Np - 1 - q), 2 * Np - q - tme), bb);
+}
+// Rank of block kv in dQ tile q of a head whose phase (kv's workers in kv's round) is
+// [lo, hi): the earlier rounds' contributions, then the phase's earlier steps.  Full mask
+// in closed form: the phase's Wp = hi - lo workers visit tile q at steps (q - c) mod N, so
+// with base = (q - lo) mod N the worker c = lo + k comes at position base - k for k <= base
+// and base + Wp - k otherwise, all workers past base being later than those up to it --
+// unless base >= Wp - 1, when every worker of the phase comes in descending order.
+DASH_HD int rank_in_phase(int causal, int N, int q, int kv, int lo, int hi, int odd) {
   if (!causal) {
     const int Wp = hi - lo, k = kv - lo;
-    int base = (q - lo) % N;
+    int base = q - lo;
     base = base < 0 ? base + N : base;
     const int in_phase = (base >= Wp - 1) ? Wp - 1 - k : (k <= base ? base - k : base + Wp - k);
     return lo + in_phase;
   }
-  return packed_count_before(causal, N, q, lo, odd) +
-         packed_count_in_phase(causal, N, q, kv, lo, hi, odd);
+  return packed_count_before(causal, N, q, lo, odd) + causal_count_in_phase(N, q, kv, lo, hi, odd);
+}
+// Rank of block kv in dQ tile q of head hd.
+DASH_HD int packed_rank(int causal, int N, int P, int hd, int q, int kv, int odd) {
+  const int W = causal ? sym_h(N, odd) : N;
+  int lo, hi;
+  packed_phase(W, P, hd, shift_worker_of(causal, N, kv, odd), &lo, &hi);
+  return rank_in_phase(causal, N, q, kv, lo, hi, odd);
 }
 
 }  // namespace dash

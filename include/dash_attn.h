@@ -32,7 +32,12 @@
  *    synchronously before anything is enqueued, launch failures as DASH_ERR_CUDA.
  *  - Device-side failures (a bounded wait that ran out, e.g. an ordering semaphore that
  *    was never released) do not hang or trap: the kernels record a code in the
- *    workspace's status word and return.  dash_attn_status() reads it.
+ *    workspace's status word and return.  dash_attn_status() reads it.  One wait gives up
+ *    after 2 s unless dash_attn_set_wait_limit() chose another limit.
+ *  - Residency: the ordered backward schedules make workers wait on workers of other CTAs,
+ *    so their tile kernel is launched cooperatively: the runtime starts it only once every
+ *    CTA of its grid (at most one per SM) can be resident, also while other kernels share
+ *    the GPU, and refuses the launch (DASH_ERR_CUDA) where that can never hold.
  */
 #ifndef DASH_ATTN_H
 #define DASH_ATTN_H
@@ -90,7 +95,8 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           S = 512 .. 16384, GQA 4:1, odd tile counts), SHIFT_FILL is the
  *                           fastest or within 2 % of the fastest (SERIAL at S = 512, plain
  *                           SHIFT on the GQA shape), and far ahead wherever the schedules
- *                           differ.  So AUTO = SHIFT_FILL. */
+ *                           differ.  So AUTO = SHIFT_FILL.
+ */
 typedef enum {
   DASH_SCHED_ATOMIC = 0,
   DASH_SCHED_SERIAL = 1,
@@ -123,10 +129,10 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
                             dash_mask_t mask, void *workspace, size_t workspace_bytes,
                             dash_stream_t stream);
 
-/* Bytes of device workspace dash_attn_bwd needs: the fp32 dQ accumulator
- * (B*H*Sp*D*4, Sp = 128*ceil(S/128)), two fp32 row vectors (B*H*Sp*4 each), the dQ
- * ordering semaphores (B*H*(Sp/128)*4) and a status block, each part 256-byte aligned;
- * 0 on bad sizes. */
+/* Bytes of device workspace dash_attn_bwd needs: a status block (256 B), the dQ ordering
+ * semaphores (one per dQ tile, B*H*(Sp/128)*4), two fp32 row vectors (B*H*Sp*4 each) and the
+ * fp32 dQ accumulator (B*H*Sp*D*4), Sp = 128*ceil(S/128), in this order, each part 256-byte
+ * aligned; 0 on bad sizes. */
 size_t dash_attn_bwd_workspace_bytes(int B, int S, int H, int D);
 
 /* Backward pass (the DASH hot path): given Q, K, V, O, dO and LSE, writes dQ, dK, dV.
@@ -175,6 +181,29 @@ dash_status_t dash_attn_bwd_stages(const void *q, const void *k, const void *v, 
  * `workspace` (fwd or bwd workspace).  DASH_OK, or DASH_ERR_TIMEOUT when a bounded wait
  * ran out on the device (the outputs of that call are then undefined). */
 dash_status_t dash_attn_status(void *workspace, dash_stream_t stream);
+/* The same, under the backward's name. */
+dash_status_t dash_attn_bwd_status(void *workspace, dash_stream_t stream);
+
+/* Limit of one device-side bounded wait (an mbarrier phase, an ordering semaphore) for the
+ * calls made after this one, process-wide: 1e-3 <= seconds <= 3600, default 2.  A wait
+ * that runs out sets the status word (DASH_ERR_TIMEOUT) and the kernel returns.  Raise it
+ * where the GPU is time-sliced with other processes for long periods. */
+dash_status_t dash_attn_set_wait_limit(double seconds);
+double dash_attn_wait_limit(void);
+
+/* The backward of dash_attn_bwd that also records the accumulation order it executed: for
+ * every (b, h, q, kv) pair the schedule visits, order_log[((b*H + h)*N + q)*N + kv] = the
+ * rank at which KV block kv's partial was added into dQ tile q (the semaphore value the
+ * addition waited for).  order_log: device int32
+ * [B, H, N, N], N = ceil(S/128); entries of masked pairs are left as they were.  Ordered
+ * schedules only (DASH_SCHED_ATOMIC records nothing).  For tests and audits. */
+dash_status_t dash_attn_bwd_order_log(const void *q, const void *k, const void *v,
+                                      const void *o, const void *dout, const float *lse,
+                                      void *dq, void *dk, void *dv, int B, int S, int H,
+                                      int group, int D, float scale, dash_mask_t mask,
+                                      dash_sched_t sched, void *workspace,
+                                      size_t workspace_bytes, int *order_log,
+                                      dash_stream_t stream);
 
 /* Allocation-free backward.  No counterpart on the DASH pages: this is a calling
  * convenience of this library.  It is for callers that cannot provide a workspace -- for
@@ -192,13 +221,17 @@ dash_status_t dash_attn_status(void *workspace, dash_stream_t stream);
  *   - All calls on a device share the array: calls that may overlap on the GPU (e.g. on
  *     unordered streams) race and corrupt each other's results; order them on one stream.
  *     Each call re-zeroes the parts that must start at zero.
- *   - Device-side status (a bounded wait that ran out) is written into the array and cannot
- *     be read through dash_attn_status; use dash_attn_bwd with a workspace to diagnose. */
+ *   - Device-side status (a bounded wait that ran out) is written into the array; read it
+ *     with dash_attn_noalloc_status. */
 #define DASH_NOALLOC_SCRATCH_BYTES (64u << 20)
 dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                                     const void *dout, const float *lse, void *dq, void *dk,
                                     void *dv, int B, int S, int H, int group, int D, float scale,
                                     dash_mask_t mask, dash_sched_t sched, dash_stream_t stream);
+/* Synchronises `stream` and reads the status word of the last dash_attn_bwd_noalloc call on
+ * the current device, as dash_attn_status does for a workspace: DASH_OK, or
+ * DASH_ERR_TIMEOUT when a bounded wait ran out (that call's outputs are undefined). */
+dash_status_t dash_attn_noalloc_status(dash_stream_t stream);
 
 /* Variable-length batches.  `batch` sequences packed along the token axis:
  *   Q, O, dO, dQ : [T, H, D]        K, V, dK, dV : [T, Hkv, D]      T = cu_seqlens[batch]

@@ -35,11 +35,13 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_workspace_sizes(L):
+    """Status block, one semaphore per dQ tile, two row vectors and the fp32 accumulator,
+    each part 256-byte aligned."""
     B, S, H, D = 2, 1024, 4, 128
     n = dash.bwd_workspace_bytes(B, S, H, D)
     rows = B * H * S
-    assert n >= 256 + rows * D * 4 + 2 * rows * 4 + B * H * (S // 128) * 4
-    assert n < 256 + rows * D * 4 + 2 * rows * 4 + B * H * (S // 128) * 4 + 4 * 256
+    need = 256 + B * H * (S // 128) * 4 + 2 * rows * 4 + rows * D * 4
+    assert need <= n < need + 4 * 256
     # a partial last tile is padded to whole tiles: S = 1000 needs the space of S = 1024
     assert dash.bwd_workspace_bytes(B, 1000, H, D) == dash.bwd_workspace_bytes(B, 1024, H, D)
     assert dash.bwd_workspace_bytes(B, S, H, 96) == 0            # unsupported head dim
@@ -60,6 +62,12 @@ def test_argument_errors_are_synchronous(L):
     fake = 1 << 20                                               # never dereferenced
     c = L.dash_attn_bwd(*([fake] * 9), 1, 384, 2, 1, 64, 0.0, 1, 6, fake, 1 << 30, null)
     assert c == 1                                                # unknown schedule
+    c = L.dash_attn_bwd_stages(*([fake] * 9), 1, 384, 2, 1, 64, 0.0, 1, 1, fake, 1 << 30, 8,
+                               null)
+    assert c == 1                                                # unknown stage bit
+    c = L.dash_attn_bwd_order_log(*([fake] * 9), 1, 384, 2, 1, 64, 0.0, 1, 1, fake, 1 << 30,
+                                  null, null)
+    assert c == 1                                                # no order log
     c = L.dash_attn_bwd(*([fake] * 9), 1, 512, 2, 1, 64, 0.0, 1, 3, fake, 16, null)
     assert c == 5                                                # workspace too small
     c = L.dash_attn_bwd(*([fake + 4] + [fake] * 8), 1, 512, 2, 1, 64, 0.0, 1, 3, fake, 1 << 30,
@@ -173,5 +181,19 @@ def test_varlen_arguments_and_workspace(L):
                                   None) == 1
     assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 3, 64, 0.0, 0, 1, fake, 1 << 30, None) == 1
     assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 1, 64, 0.0, 0, 9, fake, 1 << 30, None) == 1
+    assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 1, 64, 0.0, 0, 6, fake, 1 << 30, None) == 1
     assert L.dash_attn_fwd_varlen(*([fake] * 5), arr([2, 4]), 1, 4, 1, 64, 0.0, 0, fake, 256,
                                   None) == 1
+
+
+def test_wait_limit_setting(L):
+    """The device-side wait limit is a process-wide setting with a checked range."""
+    assert dash.wait_limit() == pytest.approx(2.0)
+    try:
+        dash.set_wait_limit(0.25)
+        assert dash.wait_limit() == pytest.approx(0.25)
+        for bad in (0.0, -1.0, 1e-4, 4000.0, float("nan")):
+            assert L.dash_attn_set_wait_limit(bad) == 1
+        assert dash.wait_limit() == pytest.approx(0.25)
+    finally:
+        dash.set_wait_limit(2.0)

@@ -1,8 +1,13 @@
 """Determinism of the ordered schedules on the GPU, as the target states it: 100 repeated
 runs of every deterministic schedule give bit-identical dQ, dK, dV, idle and while other
-kernels load the GPU from a second stream; and after a run every dQ tile's ordering
-semaphore holds exactly the number of partials the tile received (every partial went
-through its turn, none was skipped or added twice)."""
+kernels load the GPU from a second stream, at both head dims and at 128 tiles per head;
+after a run every dQ tile's ordering semaphore holds exactly the number of partials the tile
+received (every partial went through its turn, none was skipped or added twice); and the
+ordered tile kernel starts only once all of its CTAs can be resident,
+so SMs held by another kernel delay it instead of leaving its workers waiting on CTAs that
+cannot start."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -13,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 DETERMINISTIC = ["serial", "descending", "shift", "shift_fill"]
 REPEATS = 100
+SHAPES = [(2, 2048, 4, 2, 128), (1, 1024, 2, 2, 64)]
 
 
 @pytest.fixture(scope="module")
@@ -38,14 +44,11 @@ class Problem:
         return self.dq, self.dk, self.dv
 
     def semaphores(self):
-        """The [B, H, N] semaphore block of the workspace (layout: 256-byte status block,
-        then the fp32 accumulator, lse2 and Dvec, each part 256-byte aligned)."""
+        """The [B, H, N] semaphores of the workspace (layout: 256-byte status block, then
+        one int32 per dQ tile)."""
         B, S, H, _, D = self.shape
-        rows = B * H * S
-        a = lambda n: (n + 255) // 256 * 256
-        off = a(a(a(256 + rows * D * 4) + rows * 4) + rows * 4)
-        n = B * H * (S // 128)
-        return self.ws[off:off + 4 * n].view(torch.int32).view(B, H, S // 128)
+        N = S // 128
+        return self.ws[256:256 + 4 * B * H * N].view(torch.int32).view(B, H, N)
 
 
 def snapshot(outs):
@@ -53,8 +56,9 @@ def snapshot(outs):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_hundred_repeats_bit_identical(dash, causal):
-    p = Problem(dash, 2, 2048, 4, 2, 128, causal, seed=1)
+@pytest.mark.parametrize("shape", SHAPES, ids=["d128", "d64"])
+def test_hundred_repeats_bit_identical(dash, shape, causal):
+    p = Problem(dash, *shape, causal, seed=1)
     for sched in DETERMINISTIC:
         ref = snapshot(p.run(sched))
         for _ in range(REPEATS):
@@ -65,11 +69,26 @@ def test_hundred_repeats_bit_identical(dash, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_bit_identical_under_concurrent_load(dash, causal):
+def test_hundred_repeats_at_128_tiles(dash, causal):
+    """S = 16384 (N = 128 tiles, the longest sequence of the benchmark), four heads: the
+    packed schedules split heads across rounds of the grid here."""
+    p = Problem(dash, 1, 16384, 4, 4, 128, causal, seed=6)
+    for sched in DETERMINISTIC:
+        ref = snapshot(p.run(sched))
+        for _ in range(REPEATS):
+            out = p.run(sched)
+            for a, b in zip(out, ref):
+                assert torch.equal(a, b), sched
+        p.dash.status(p.ws)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES, ids=["d128", "d64"])
+def test_bit_identical_under_concurrent_load(dash, shape, causal):
     """A second stream keeps the GPU busy with matrix products while the backward runs on
     the current stream: the persistent CTAs start late and at different times, the results
     must not change."""
-    p = Problem(dash, 2, 2048, 4, 2, 128, causal, seed=2)
+    p = Problem(dash, *shape, causal, seed=2)
     side = torch.cuda.Stream()
     a = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
     sink = torch.empty_like(a)
@@ -77,9 +96,9 @@ def test_bit_identical_under_concurrent_load(dash, causal):
         torch.cuda.synchronize()
         ref = snapshot(p.run(sched))
         torch.cuda.synchronize()
-        for i in range(REPEATS // 4):
+        for i in range(REPEATS):
             with torch.cuda.stream(side):
-                for _ in range(8):
+                for _ in range(4):
                     torch.matmul(a, a, out=sink)
             out = p.run(sched)
             for x, y in zip(out, ref):
@@ -88,7 +107,7 @@ def test_bit_identical_under_concurrent_load(dash, causal):
         p.dash.status(p.ws)
 
 
-@pytest.mark.parametrize("shape", [(2, 2048, 4, 2, 128), (1, 1024, 2, 2, 64)])
+@pytest.mark.parametrize("shape", SHAPES, ids=["d128", "d64"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_every_partial_takes_its_turn(dash, shape, causal):
     p = Problem(dash, *shape, causal, seed=0)
@@ -111,3 +130,32 @@ def test_auto_runs_the_resolved_schedule(dash, shape, causal):
     p.dash.status(p.ws)
     for a, b in zip(out, ref):
         assert torch.equal(a, b), want
+
+
+@pytest.mark.parametrize("sched", ["shift_fill", "serial"])
+def test_waits_for_sms_held_by_another_kernel(dash, sched):
+    """Kernels on other streams hold some SMs for 0.5 s while the device-side wait limit is
+    0.2 s.  A grid started with only part of its CTAs resident would leave its first
+    workers waiting on CTAs that cannot start, and the wait would run out; the ordered
+    tile kernel is launched so that it starts only when every CTA fits.  It must finish
+    with DASH_OK, after the holders, with the same bits as on an idle GPU."""
+    p = Problem(dash, 1, 4096, 8, 8, 128, False, seed=8)
+    ref = snapshot(p.run(sched))
+    torch.cuda.synchronize()
+    rate = 2.07e9  # the GB300's maximum SM clock: a lower clock only sleeps longer
+    holders = [torch.cuda.Stream() for _ in range(16)]
+    try:
+        dash.set_wait_limit(0.2)
+        t0 = time.time()
+        for s in holders:
+            with torch.cuda.stream(s):
+                torch.cuda._sleep(int(0.5 * rate))
+        out = p.run(sched)
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+        p.dash.status(p.ws)
+    finally:
+        dash.set_wait_limit(2.0)
+    assert elapsed >= 0.4, elapsed
+    for x, y in zip(out, ref):
+        assert torch.equal(x, y), sched

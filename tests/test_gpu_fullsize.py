@@ -1,8 +1,10 @@
 """Parity at the benchmark's full sizes, in the launch configuration bench.py times: the
-largest point of each configuration, the CUDA path (forward, then the backward with the
-bench's schedule and with the atomic variant) against the fp64 oracle on sampled rows of one
-(batch, kv head) group -- every row the oracle restates is computed from the definitions at
-full length (LSE and Dvec over all rows, then the sampled dQ, dK, dV rows)."""
+largest point of each configuration, the CUDA path (forward, then the backward with every
+schedule the bench times, ordered and atomic) against the fp64 oracle on sampled rows of
+three (batch, kv head) groups -- the first, the last, and one whose workers the packed
+schedules split across two rounds of the grid -- every row the oracle restates computed
+from the definitions at full length (LSE and Dvec over all rows, then the sampled dQ, dK, dV
+rows)."""
 import numpy as np
 import pytest
 import torch
@@ -14,6 +16,7 @@ pytestmark = pytest.mark.gpu
 
 REL_FRO = 1e-2
 MAX_ABS = 2e-2
+SCHEDULES = ["atomic", "serial", "descending", "shift", "shift_fill"]
 CONFIGS = [  # (name, B, S, H, Hkv, D, causal, schedule timed by bench.py)
     ("full_h16_d128", 1, 16384, 16, 16, 128, False, "shift_fill"),
     ("causal_h32_d128", 1, 16384, 32, 32, 128, True, "shift_fill"),
@@ -43,26 +46,39 @@ def close(name, got, ref):
     assert rel <= REL_FRO and mx <= MAX_ABS, f"{name}: rel_fro={rel:.3e} max={mx:.3e}"
 
 
+def sampled_groups(dash, causal, N, B, Hkv):
+    """(b, g) groups to compare: the first, the last, and a head the packed schedule splits
+    across rounds of the grid (if any)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    heads = B * Hkv
+    W = dash.sched_workers("shift_fill", causal, N)
+    grid = dash.sched_grid("shift_fill", causal, N, heads, sms)
+    split = [hd for hd in range(1, heads - 1) if (hd * W) // grid != (hd * W + W - 1) // grid]
+    picks = [0, heads - 1] + split[:1]
+    return [divmod(hd, Hkv) for hd in dict.fromkeys(picks)]
+
+
 @pytest.mark.parametrize("cfg", CONFIGS, ids=[c[0] for c in CONFIGS])
 def test_full_size_sampled_rows_match_oracle(dash, cfg):
-    name, B, S, H, Hkv, D, causal, sched = cfg
+    name, B, S, H, Hkv, D, causal, _ = cfg
     host = make_qkv_do(B, S, H, Hkv, D, seed=0)
     q, k, v, do = (t.cuda() for t in host)
     o, lse = dash.fwd(q, k, v, causal=causal, check=True)
     ws = torch.empty(dash.bwd_workspace_bytes(B, S, H, D), dtype=torch.uint8, device="cuda")
-    outs = {}
-    for s in (sched, "atomic"):
+    G = H // Hkv
+    groups = sampled_groups(dash, causal, S // 128, B, Hkv)
+    assert len(groups) >= 2
+    qr, kr = sample_rows(S, 1), sample_rows(S, 2)
+    refs = {bg: oracle.attn_bwd_rows(*host, causal, bg[0], bg[1], qr, kr) for bg in groups}
+    for s in SCHEDULES:
         grads = dash.bwd(q, k, v, o, do, lse, causal=causal, schedule=s, workspace=ws)
         dash.status(ws)
-        outs[s] = [t.detach().to(torch.float64).cpu().numpy() for t in grads]
-    G = H // Hkv
-    b, g = B - 1, Hkv - 1  # the last group: every earlier batch/head precedes it in memory
-    qr, kr = sample_rows(S, 1), sample_rows(S, 2)
-    sq, sk, sv = oracle.attn_bwd_rows(*host, causal, b, g, qr, kr)
-    for s, (dq, dk, dv) in outs.items():
-        close(f"{name} {s} dQ", dq[b, qr][:, g * G:(g + 1) * G], sq)
-        close(f"{name} {s} dK", dk[b, kr, g], sk)
-        close(f"{name} {s} dV", dv[b, kr, g], sv)
+        for b, g in groups:
+            sq, sk, sv = refs[(b, g)]
+            rows_q = grads[0][b, qr][:, g * G:(g + 1) * G].to(torch.float64).cpu().numpy()
+            close(f"{name} {s} ({b},{g}) dQ", rows_q, sq)
+            close(f"{name} {s} ({b},{g}) dK", grads[1][b, kr, g].to(torch.float64).cpu().numpy(), sk)
+            close(f"{name} {s} ({b},{g}) dV", grads[2][b, kr, g].to(torch.float64).cpu().numpy(), sv)
 
 
 @pytest.mark.parametrize("causal,S", [(False, 160 * 128), (True, 320 * 128), (True, 319 * 128)])
