@@ -59,8 +59,8 @@ WORKLOADS = {
         desc="full-mask attention backward, B=1, H=2, S=512, D=64 (4 KV blocks)",
         H=2, Hkv=2, D=64, causal=False, tokens=512, seqs=[512], schedule="shift_fill", ref_S=512),
 }
-SCHEDULES = ["atomic", "serial", "descending", "shift", "shift_fill"]
-DETERMINISTIC = ["serial", "descending", "shift", "shift_fill"]
+SCHEDULES = ["atomic", "serial", "descending", "shift", "shift_fill", "shift_dual"]
+DETERMINISTIC = ["serial", "descending", "shift", "shift_fill", "shift_dual"]
 FALLBACK_PEAK_TFLOPS = 1900.0   # only if the measured-peaks file is absent
 PROFILE = os.path.join(ROOT, "profiles", "bwd_tile_kernel_full_h16_d128.md")
 KERNEL_SOURCES = ["bwd.cu", "ptx.cuh", "sched.cuh", "common.cuh"]

@@ -27,7 +27,11 @@ __all__ = ["fwd", "bwd", "bwd_workspace_bytes", "fwd_workspace_bytes", "status",
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdash_attn.so")
 
-SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3, "shift_fill": 4, "auto": 5}
+SCHEDULES = {"atomic": 0, "serial": 1, "descending": 2, "shift": 3, "shift_fill": 4, "auto": 5,
+             "shift_dual": 6}
+# accumulation strands per dQ tile (the atomic variant adds in no order)
+STRANDS = {"atomic": 1, "serial": 1, "descending": 1, "shift": 1, "shift_fill": 1,
+           "shift_dual": 2}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "device-side wait timed out", 5: "workspace missing or too small"}
 EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_workspace_bytes",
@@ -111,7 +115,7 @@ def lib() -> ctypes.CDLL:
         L.dash_sched_grid.restype = i
         L.dash_sched_packed_rank.argtypes = [i, i, i, i, i, i, i]
         L.dash_sched_packed_rank.restype = i
-        L.dash_sched_resolve.argtypes = [i, i, i]
+        L.dash_sched_resolve.argtypes = [i, i, i, i, i]
         L.dash_sched_resolve.restype = i
         _lib = L
         return L
@@ -192,7 +196,8 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, schedule: str = "shift",
     """Attention backward: returns (dQ, dK, dV) bf16.  ``schedule`` is one of
     ``atomic`` (non-deterministic reference), ``serial``, ``descending``, ``shift``,
     ``shift_fill`` (packed shift: all SMs busy, heads split across rounds run in phases),
-    ``auto`` (the measured-fastest deterministic schedule, see ``sched_resolve``).
+    ``auto`` (the measured-fastest deterministic schedule, see ``sched_resolve``),
+    ``shift_dual`` (packed shift, each dQ tile accumulated in two strands; D = 128).
     ``stages`` (PROLOGUE | TILES | EPILOGUE) launches only part of the work, in order, on
     the same workspace (for timing the tile kernel on its own)."""
     import torch
@@ -261,9 +266,10 @@ def wait_limit() -> float:
     return float(lib().dash_attn_wait_limit())
 
 
-def sched_resolve(schedule: str, causal: bool, N: int) -> str:
-    """The schedule the backward runs for ``schedule`` (``auto`` resolved) at N tiles."""
-    r = lib().dash_sched_resolve(SCHEDULES[schedule], int(bool(causal)), N)
+def sched_resolve(schedule: str, causal: bool, N: int, D: int = 128, group: int = 1) -> str:
+    """The schedule the backward runs for ``schedule`` (``auto`` resolved) at N tiles, head
+    dim D and ``group`` query heads per KV head."""
+    r = lib().dash_sched_resolve(SCHEDULES[schedule], int(bool(causal)), D, N, group)
     if r < 0:
         raise ValueError("unsupported schedule arguments")
     return {v: k for k, v in SCHEDULES.items()}[r]

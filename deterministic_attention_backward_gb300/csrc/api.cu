@@ -100,7 +100,8 @@ struct BwdWorkspace {
 
 // [status 256 B][semaphores][lse2][Dvec][dQ accumulator], each part 256-byte aligned; the
 // status block and the semaphores are contiguous so that one clear covers both.  Row arrays
-// are per tile: S padded up to N*128 rows per (b, h).
+// are per tile: S padded up to N*128 rows per (b, h).  Semaphores and accumulator have room
+// for kMaxStrands strands per dQ tile (a call with K strands uses [B,H,N][K]...).
 BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
   BwdWorkspace w{};
   const size_t ntiles = (size_t)B * H * tiles(S);
@@ -110,15 +111,15 @@ BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
   w.status = reinterpret_cast<uint32_t *>(base + off);
   off += kStatusBytes;
   w.sem = reinterpret_cast<int *>(base + off);
-  w.sem_bytes = ntiles * 4;
+  w.sem_bytes = ntiles * 4 * dash::kMaxStrands;
   off = align256(off + w.sem_bytes);
   w.lse2 = reinterpret_cast<float *>(base + off);
   off = align256(off + rows * 4);
   w.dvec = reinterpret_cast<float *>(base + off);
   off = align256(off + rows * 4);
   w.dqacc = reinterpret_cast<float *>(base + off);
-  w.dqacc_bytes = rows * D * 4;
-  off = align256(off + w.dqacc_bytes);
+  w.dqacc_bytes = rows * D * 4;  // one strand
+  off = align256(off + w.dqacc_bytes * dash::kMaxStrands);
   w.total = off;
   return w;
 }
@@ -134,17 +135,22 @@ int g_trace_cta = 0;
 // How the backward tile kernel's grid is used: the workers of all heads, head-major, dealt
 // round-robin to `grid` CTAs.
 struct LaunchPlan {
-  int sched, workers, grid, packed;
+  int sched, workers, grid, packed, strands;
 };
 
-bool sched_known(int sched) { return sched >= DASH_SCHED_ATOMIC && sched <= DASH_SCHED_AUTO; }
+bool sched_known(int sched) {
+  return (sched >= DASH_SCHED_ATOMIC && sched <= DASH_SCHED_AUTO) || sched == DASH_SCHED_SHIFT_DUAL;
+}
 
-// DASH_SCHED_AUTO: SHIFT_FILL (the measured choice for every mask, head dim and length;
-// see the header).
-int resolve_sched(int sched, int mask, int N) {
-  (void)mask;
+// DASH_SCHED_AUTO: the deterministic schedule measured fastest on GB300 for the mask, head
+// dim D, tile count N and group size G (the table is in the header).  D = 0 asks for the
+// traversal only (the schedule queries): SHIFT_FILL, whose tables DASH_SCHED_SHIFT_DUAL
+// shares.
+int resolve_sched(int sched, int mask, int D, int N, int G) {
   (void)N;
-  return sched == DASH_SCHED_AUTO ? DASH_SCHED_SHIFT_FILL : sched;
+  (void)G;
+  if (sched != DASH_SCHED_AUTO) return sched;
+  return (D == 128 && mask == DASH_MASK_FULL) ? DASH_SCHED_SHIFT_DUAL : DASH_SCHED_SHIFT_FILL;
 }
 
 // False when plain SHIFT cannot have every worker of a head resident at once.  The packed
@@ -155,7 +161,8 @@ bool make_plan(int sched, int causal, int N, int heads, int sms, LaunchPlan *pl)
   pl->workers = dash::sched_workers(pl->sched, causal, N, N & 1);
   const long long total = (long long)heads * pl->workers;
   pl->grid = (int)(total < sms ? total : sms);
-  pl->packed = sched == DASH_SCHED_SHIFT_FILL;
+  pl->packed = sched == DASH_SCHED_SHIFT_FILL || sched == DASH_SCHED_SHIFT_DUAL;
+  pl->strands = sched == DASH_SCHED_SHIFT_DUAL ? 2 : 1;
   return !(sched == DASH_SCHED_SHIFT && pl->workers > sms);
 }
 
@@ -236,7 +243,7 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   if (st != DASH_OK) return st;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
   if (!sched_known(sched)) return DASH_ERR_INVALID;
-  sched = (dash_sched_t)resolve_sched(sched, mask, tiles(S));
+  sched = (dash_sched_t)resolve_sched(sched, mask, D, tiles(S), group);
   const void *ptrs[] = {q, k, v, o, dout, dq, dk, dv};
   for (const void *ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return DASH_ERR_INVALID;
@@ -254,6 +261,8 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   // every worker of a head must be resident at once for the shift schedules
   if (!make_plan(sched, causal, N, B * Hkv, dev.sms, &plan)) return DASH_ERR_UNSUPPORTED;
   const bool ordered = sched != DASH_SCHED_ATOMIC;
+  const int K = plan.strands;
+  if (K > 1 && D != 128) return DASH_ERR_UNSUPPORTED;  // the two-strand kernel is D = 128
 
   CUtensorMap tq, tk, tv, tdo;
   if (!make_bshd_map(&tq, q, B, S, H, D) || !make_bshd_map(&tk, k, B, S, Hkv, D) ||
@@ -267,7 +276,7 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
     // status word and semaphores are contiguous; the accumulator separately
     if ((keep_status ? cudaMemsetAsync(w.sem, 0, w.sem_bytes, s)
                      : cudaMemsetAsync(w.status, 0, kStatusBytes + w.sem_bytes, s)) != cudaSuccess ||
-        cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes, s) != cudaSuccess)
+        cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes * K, s) != cudaSuccess)
       return DASH_ERR_CUDA;
     // a partial last tile: its padding rows of lse2 / Dvec must read as zero
     if ((S % kTile) &&
@@ -311,11 +320,13 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   p.trace_cta = 0;
 #endif
   if ((stages & DASH_BWD_TILES) &&
-      dash::launch_bwd(D, ordered, causal ? (((N & 1) && plan.sched == dash::kShift) ? 2 : 1) : 0,
+      dash::launch_bwd(D, ordered,
+                       (causal ? (((N & 1) && plan.sched == dash::kShift) ? 2 : 1) : 0) |
+                           (K > 1 ? 4 : 0),
                        tq, tk, tv, tdo, p, plan.grid, s) != cudaSuccess)
     return DASH_ERR_CUDA;
   if ((stages & DASH_BWD_EPILOGUE) &&
-      dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, s) !=
+      dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, K, s) !=
           cudaSuccess)
     return DASH_ERR_CUDA;
   return DASH_OK;
@@ -425,7 +436,7 @@ dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, 
     const int S = cu_seqlens[b + 1] - cu_seqlens[b];
     if (S == 0) continue;
     if ((st = check_sizes(1, S, H, group, D)) != DASH_OK) return st;
-    const int N = tiles(S), rs = resolve_sched(sched, mask, N);
+    const int N = tiles(S), rs = resolve_sched(sched, mask, D, N, group);
     LaunchPlan plan;
     if (!make_plan(rs, mask == DASH_MASK_CAUSAL, N, Hkv, dev.sms, &plan))
       return DASH_ERR_UNSUPPORTED;
@@ -497,13 +508,15 @@ void dash_debug_set_trace(unsigned long long *buf, int cta) {
 // ------------------------------------------------------------------ schedule queries
 static bool sched_args_ok(int &sched, int mask, int N) {
   if (!sched_known(sched) || (mask != 0 && mask != 1) || N <= 0) return false;
-  sched = resolve_sched(sched, mask, N);
+  sched = resolve_sched(sched, mask, 0, N, 1);
   return true;
 }
 
-int dash_sched_resolve(int sched, int mask, int N) {
-  if (!sched_args_ok(sched, mask, N)) return -1;
-  return sched;
+int dash_sched_resolve(int sched, int mask, int D, int N, int group) {
+  if (!sched_known(sched) || (mask != 0 && mask != 1) || N <= 0 || group <= 0 ||
+      (D != 64 && D != 128))
+    return -1;
+  return resolve_sched(sched, mask, D, N, group);
 }
 
 int dash_sched_grid(int sched, int mask, int N, int heads, int sms) {
@@ -530,14 +543,14 @@ int dash_sched_workers(int sched, int mask, int N) {
 }
 
 int dash_sched_segments(int sched, int mask, int N, int worker) {
-  sched = resolve_sched(sched, mask, N);
+  sched = resolve_sched(sched, mask, 0, N, 1);
   const int W = dash_sched_workers(sched, mask, N);
   if (W < 0 || worker < 0 || worker >= W) return -1;
   return dash::sched_segments(dash::traversal(sched, mask, N), mask, N, worker, N & 1);
 }
 
 int dash_sched_steps(int sched, int mask, int N, int worker, int segment) {
-  sched = resolve_sched(sched, mask, N);
+  sched = resolve_sched(sched, mask, 0, N, 1);
   const int nseg = dash_sched_segments(sched, mask, N, worker);
   if (nseg < 0 || segment < 0 || segment >= nseg) return -1;
   return dash::seg_steps(dash::traversal(sched, mask, N), mask, N, worker, segment, N & 1);
@@ -545,7 +558,7 @@ int dash_sched_steps(int sched, int mask, int N, int worker, int segment) {
 
 int dash_sched_step(int sched, int mask, int N, int worker, int segment, int step, int *kv,
                     int *q, int *rank) {
-  sched = resolve_sched(sched, mask, N);
+  sched = resolve_sched(sched, mask, 0, N, 1);
   const int n = dash_sched_steps(sched, mask, N, worker, segment);
   if (n < 0 || step < 0 || step >= n) return -1;
   const int t = dash::traversal(sched, mask, N);

@@ -2,7 +2,8 @@
 //   preprocess:  Dvec[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]   (fp32)
 //                lse2[b,h,i] = LSE[b,h,i] * log2(e)              (exp2-domain LSE)
 //                (both [B,H,N*128]: each (b,h) padded to whole tiles; padding stays zero)
-//   dq_convert:  dQ[b,i,h,:] = bf16_rne(scale * dQacc)            (tile-native -> BSHD, i < S)
+//   dq_convert:  dQ[b,i,h,:] = bf16_rne(scale * (acc_0 [+ acc_1]))  (the tile's accumulation
+//                strands in ascending order; tile-native -> BSHD, i < S)
 #include "common.cuh"
 
 namespace dash {
@@ -58,8 +59,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16 *__
 }
 
 // One thread per 4 output elements; the 4-column chunk index runs fastest so a warp
-// writes contiguous bf16 rows.  dQacc layout: [B,H,N][D/4][128][4].
-template <int D>
+// writes contiguous bf16 rows.  dQacc layout: [B,H,N][K][D/4][128][4], K strands.
+template <int D, int K>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
                                                          __nv_bfloat16 *__restrict__ dq,
                                                          float scale, int B, int S, int H) {
@@ -76,7 +77,12 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
     const int h = (int)(bh % H);
     const int b = (int)(bh / H);
     if (i * kTile + r >= S) continue;  // padding rows of a partial last tile
-    const float4 v = *reinterpret_cast<const float4 *>(acc + ((t * C4 + c4) * kTile + r) * 4);
+    const float *tb = acc + t * K * (C4 * kTile * 4);
+    float4 v = *reinterpret_cast<const float4 *>(tb + ((size_t)c4 * kTile + r) * 4);
+    if constexpr (K == 2) {  // strand 0 + strand 1
+      const float4 w = *reinterpret_cast<const float4 *>(tb + ((size_t)(C4 + c4) * kTile + r) * 4);
+      v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+    }
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
     __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
     uint2 packed;
@@ -108,13 +114,20 @@ cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
 }
 
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B, int S,
-                              int H, int D, cudaStream_t stream) {
+                              int H, int D, int strands, cudaStream_t stream) {
   const long long work = (long long)B * H * ((S + kTile - 1) / kTile) * kTile * (D / 4);
   const int grid = grid_for(work, 256, 152 * 32);
-  if (D == 64)
-    dq_convert_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
-  else
-    dq_convert_kernel<128><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+  if (D == 64) {
+    if (strands == 2)
+      dq_convert_kernel<64, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+    else
+      dq_convert_kernel<64, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+  } else {
+    if (strands == 2)
+      dq_convert_kernel<128, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+    else
+      dq_convert_kernel<128, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+  }
   return cudaGetLastError();
 }
 

@@ -58,9 +58,11 @@
 namespace dash {
 namespace {
 
-// The tile kernel's compile-time mask mode (0 full, 1 causal, 2 causal with an odd tile
-// count under Symmetric Shift) and the `odd` of the schedule it implies.
-__host__ __device__ constexpr int odd_of(int mode) { return mode == 2 ? 1 : 0; }
+// The tile kernel's compile-time mode: bits 0-1 the mask (0 full, 1 causal, 2 causal with an
+// odd tile count under Symmetric Shift), bit 2 the two-strand accumulation of
+// DASH_SCHED_SHIFT_DUAL (D = 128, ordered).  `odd` of the schedule the mode implies:
+__host__ __device__ constexpr int odd_of(int mode) { return (mode & 3) == 2 ? 1 : 0; }
+__host__ __device__ constexpr bool dual_of(int mode) { return (mode & 4) != 0; }
 
 // Depth of the ring of mbarriers through which the semaphore poller hands a dQ tile's turn
 // to the epilogue (D = 128, ordered variant).
@@ -93,9 +95,12 @@ struct BwdLayout {
   // counter, so it adds no shared-memory loads beside the softmax-gradient warps' traffic
   // (measured: +3 % at D = 128).  At D = 64 the counter measured faster.
   static constexpr bool kTurnRing = DET && D == 128;
-  static constexpr int kNumBars = 2 * kStages + 15 + (kTurnRing ? 2 * kTurns : 0);
+  // two-strand mode: a third ring (the epilogue's additions issued, for the releaser warp)
+  // and the ranks of the ring's steps (misc words from offRanks)
+  static constexpr int kNumBars = 2 * kStages + 15 + (kTurnRing ? 3 * kTurns : 0);
   static constexpr int offMisc = offBar + kNumBars * 8;
-  static constexpr int kBytes = offMisc + 32;
+  static constexpr int offRanks = offMisc + 32;
+  static constexpr int kBytes = offRanks + (kTurnRing ? 4 * kTurns : 0);
   static constexpr uint32_t tS = 0, tDP = 128, tDK = 256, tDV = 256 + D;
   static constexpr uint32_t tDQ = (D == 64) ? 384 : 128;
   static constexpr bool kDQOwnCols = (D == 64);  // dQ partial does not alias dP^T
@@ -116,12 +121,14 @@ struct RegSplit {
   static_assert(kCtl + 2 * kSoftmax + kEpi == 4 * kLaunch, "register split must sum to the launch");
 };
 
-// Pacing of the unordered dQ reductions: a burst of red.global fills the SM's memory
-// instruction queue and stalls the tcgen05 and shared-memory traffic of the other warps
-// behind it, so the atomic variant's epilogue sleeps briefly after every kRedPaceEvery
-// vector reductions (measured: +22% at S = 16k, full mask, D = 128).  The ordered
-// reductions are not paced: spreading them out lengthens the chain of dQ-tile turns by
-// more than the stalls cost.
+// Pacing of the dQ reductions: a burst of red.global fills the SM's memory instruction
+// queue and stalls the tcgen05 and shared-memory traffic of the other warps behind it, so
+// the epilogue sleeps briefly after every kRedPaceEvery vector reductions (measured: +22% at
+// S = 16k, full mask, D = 128, atomic variant).  The single-chain ordered reductions are not
+// paced: a dQ tile's next contributor follows one lock step later, and spreading them out
+// lengthens that chain of turns by more than the stalls cost.  The two-strand mode paces
+// them: a strand's next contributor follows two lock steps later (measured: the two strands
+// gain nothing unpaced, and 150-250 ns every 4 reductions all give the same +16 %).
 constexpr int kRedPaceEvery = 4;
 constexpr uint32_t kRedPaceNs = 200;
 
@@ -130,7 +137,7 @@ constexpr uint32_t kRedPaceNs = 200;
 // causal builds (measured: folding it there too cost 7 % on GQA shapes).
 template <int MODE>
 __device__ __forceinline__ int mode_causal(const BwdParams &p) {
-  return MODE == 0 ? 0 : p.causal;
+  return (MODE & 3) == 0 ? 0 : p.causal;
 }
 
 struct Plan {
@@ -162,7 +169,7 @@ __device__ __forceinline__ Unit decode_unit(const BwdParams &p, const Plan &pl, 
 template <int D, bool DET>
 struct Bars {
   uint64_t *full, *empty, *kv_full, *kv_empty, *s_full, *p_ready, *dp_full, *pds, *g5_done,
-      *dq_empty, *dkv_full, *dkv_empty, *drain, *turn_full, *turn_empty;
+      *dq_empty, *dkv_full, *dkv_empty, *drain, *turn_full, *turn_empty, *added;
   __device__ explicit Bars(uint8_t *smem) {
     using L = BwdLayout<D, DET>;
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + L::offBar);
@@ -182,6 +189,7 @@ struct Bars {
     drain = b + 14;
     turn_full = L::kTurnRing ? b + 15 : nullptr;  // [kTurns]: the step's semaphore reached its rank
     turn_empty = L::kTurnRing ? b + 15 + kTurns : nullptr;  // [kTurns]: the step was released
+    added = L::kTurnRing ? b + 15 + 2 * kTurns : nullptr;  // [kTurns]: additions issued (dual)
   }
 };
 
@@ -591,6 +599,8 @@ __device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, con
 template <int D, bool DET, int MODE>
 __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &ab) {
   using L = BwdLayout<D, DET>;
+  constexpr bool kDual = dual_of(MODE);
+  volatile int *ranks = reinterpret_cast<volatile int *>(smem + L::offRanks);
   const int lane = lane_id();
   uint32_t *seen = reinterpret_cast<uint32_t *>(smem + L::offMisc + 16);
   const Bars<D, DET> bar(smem);
@@ -608,20 +618,69 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
         const int rank = step_rank<MODE>(p, pl, o, q, kv);
         for (int g = 0; g < p.G; ++g, ++it) {
           const int h = un.hkv * p.G + g;
-          const int *sem = p.sem + (size_t)(un.b * p.H + h) * p.N + q;
+          // the step's semaphore: the tile's, or (two strands) that of strand rank % 2, on which
+          // the partial's turn comes when the strand has counted its rank / 2 earlier partials
+          const size_t ptile = (size_t)(un.b * p.H + h) * p.N + q;
+          const int *sem = kDual ? p.sem + ptile * 2 + (rank & 1) : p.sem + ptile;
+          const int want = kDual ? rank >> 1 : rank;
           int ok = 1;
           if (lane == 0) {
             if constexpr (L::kTurnRing) {
               // the slot is free once the epilogue has released the step kTurns earlier
               const uint32_t slot = it % kTurns, wrap = (it / kTurns) & 1;
-              ok = (mbar_wait(&bar.turn_empty[slot], wrap ^ 1, ab) && sem_wait(sem, rank, ab)) ? 1 : 0;
-              if (ok) mbar_arrive(&bar.turn_full[slot]);
+              ok = (mbar_wait(&bar.turn_empty[slot], wrap ^ 1, ab) && sem_wait(sem, want, ab)) ? 1 : 0;
+              if (ok) {
+                if constexpr (kDual) ranks[slot] = rank;
+                mbar_arrive(&bar.turn_full[slot]);
+              }
             } else {
-              ok = sem_wait(sem, rank, ab) ? 1 : 0;
+              ok = sem_wait(sem, want, ab) ? 1 : 0;
               if (ok) st_release_cta_shared(seen, it + 1);
             }
             // audit record of the executed order (dash_attn_bwd_order_log)
-            if (ok && p.order_log) p.order_log[(size_t)(sem - p.sem) * p.N + kv] = rank;
+            if (ok && p.order_log) p.order_log[ptile * p.N + kv] = rank;
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        }
+      }
+    }
+  }
+}
+
+// Releaser (warp 2 in the two-strand mode, after it has allocated the tensor memory): once
+// the epilogue warpgroup has issued a step's reductions (its threads met at a named barrier,
+// then one of them arrived on the step's `added` slot), advances the semaphore of the step's
+// dQ tile and strand by one with gpu-scope release semantics -- which orders every one of
+// those reductions before it -- and frees the turn-ring slot for the poller.  The release
+// waits until the reductions are performed; done here, that wait does not hold the
+// epilogue, which goes on to drain the next dQ partial (measured: +16 % together with the
+// paced reductions at S = 16k, full mask; neither helps alone).
+template <int D, bool DET, int MODE>
+__device__ void bwd_releaser(const BwdParams &p, uint8_t *smem, const Bars<D, DET> &bar,
+                             const Abort &ab) {
+  using L = BwdLayout<D, DET>;
+  const int lane = lane_id();
+  const volatile int *ranks = reinterpret_cast<const volatile int *>(smem + L::offRanks);
+  uint32_t it = 0;
+  const Plan pl = cta_plan(p);
+  for (int u = pl.first; u < pl.nunits; u += pl.stride) {
+    const Unit un = decode_unit(p, pl, u);
+    const int nseg = sched_segments(pl.sched, mode_causal<MODE>(p), p.N, un.w, odd_of(MODE));
+    for (int seg = 0; seg < nseg; ++seg) {
+      const int nsteps = seg_steps(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, odd_of(MODE));
+      for (int t = 0; t < nsteps; ++t) {
+        const int q = step_q(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, t, odd_of(MODE));
+        for (int g = 0; g < p.G; ++g, ++it) {
+          const size_t ptile = (size_t)(un.b * p.H + un.hkv * p.G + g) * p.N + q;
+          int ok = 1;
+          if (lane == 0) {
+            const uint32_t slot = it % kTurns;
+            ok = mbar_wait(&bar.added[slot], (it / kTurns) & 1, ab) ? 1 : 0;
+            if (ok) {
+              // the slot's rank stays valid until turn_empty lets the poller reuse the slot
+              red_release_add(p.sem + ptile * 2 + (ranks[slot] & 1), 1);
+              mbar_arrive(&bar.turn_empty[slot]);
+            }
           }
           if (!__shfl_sync(0xffffffffu, ok, 0)) return;
         }
@@ -634,6 +693,7 @@ template <int D, bool DET, int MODE>
 __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
                              const Abort &ab) {
   using L = BwdLayout<D, DET>;
+  constexpr bool kDual = dual_of(MODE);
   const int warp = warp_id(), lane = lane_id();
   const int et = threadIdx.x - 12 * 32;  // 0..127
   const int quad = warp & 3;
@@ -644,11 +704,13 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
   volatile int *decision = reinterpret_cast<volatile int *>(smem + L::offMisc + 8);
   uint32_t it = 0, seg_it = 0, dec = 0;
   bool ok = true;
-  auto agree = [&](bool mine) -> bool {
-    if (et == 0) decision[dec & 1] = mine ? 1 : 0;
+  auto agree_int = [&](int mine) -> int {
+    if (et == 0) decision[dec & 1] = mine;
     named_bar_sync(1, 128);
-    return decision[dec++ & 1] != 0;
+    return decision[dec++ & 1];
   };
+  auto agree = [&](bool mine) -> bool { return agree_int(mine ? 1 : 0) != 0; };
+  const volatile int *ranks = reinterpret_cast<const volatile int *>(smem + L::offRanks);
   const uint32_t *seen = reinterpret_cast<const uint32_t *>(smem + L::offMisc + 16);
   constexpr bool kBulk = L::kBulkDQ && !DET;
   const Plan pl = cta_plan(p);
@@ -663,7 +725,6 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           const int h = un.hkv * p.G + g;
           const int q = step_q(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, t, odd_of(MODE));
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
-          int *sem = p.sem + tile_idx;
           if (!agree(et == 0 ? mbar_wait(bar.g5_done, it & 1, ab) : true)) {
             ok = false;
             break;
@@ -679,8 +740,8 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           __syncwarp();
           if (lane == 0) mbar_arrive(bar.dq_empty);
           if (et == 0) DASH_TRACE(p, 15);
-          float *tile = p.dqacc + tile_idx * (size_t)(kTile * D);
           if constexpr (kBulk) {
+            float *tile = p.dqacc + tile_idx * (size_t)(kTile * D);
             // the partial into the staging tile (same tile-native layout as the accumulator;
             // the previous reduction finished reading it before thread 0 left the last step)
             float4 *stg = reinterpret_cast<float4 *>(smem + L::offStg);
@@ -705,16 +766,24 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           }
           // the semaphore counts the partials added so far: the contributor of rank r goes
           // once rank r-1 has released it; the poller warp has been watching it
-          bool turn = true;
+          // (two strands: thread 0 also reads the partial's rank, and the warpgroup learns
+          // its strand with the turn)
+          int turn = 1;
           if constexpr (L::kTurnRing) {
-            if (et == 0) turn = mbar_wait(&bar.turn_full[it % kTurns], (it / kTurns) & 1, ab);
+            if (et == 0)
+              turn = mbar_wait(&bar.turn_full[it % kTurns], (it / kTurns) & 1, ab)
+                         ? (kDual ? 1 + (ranks[it % kTurns] & 1) : 1)
+                         : 0;
           } else if constexpr (DET) {
-            if (et == 0) turn = counter_wait(seen, it + 1, ab);
+            if (et == 0) turn = counter_wait(seen, it + 1, ab) ? 1 : 0;
           }
-          if (DET && !agree(turn)) {
+          if (DET) turn = agree_int(turn);
+          if (turn == 0) {
             ok = false;
             break;
           }
+          const size_t acc_idx = kDual ? tile_idx * 2 + (turn - 1) : tile_idx;
+          float *tile = p.dqacc + acc_idx * (size_t)(kTile * D);
           if (et == 0) DASH_TRACE(p, 16);
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
@@ -724,15 +793,19 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
               red_add_v4(tile + ((size_t)c4 * kTile + r) * 4, __uint_as_float(v[ch][4 * j]),
                          __uint_as_float(v[ch][4 * j + 1]), __uint_as_float(v[ch][4 * j + 2]),
                          __uint_as_float(v[ch][4 * j + 3]));
-              if (!DET && (ch * 8 + j + 1) % kRedPaceEvery == 0 && ch * 8 + j + 1 < D / 4)
+              if ((!DET || kDual) && (ch * 8 + j + 1) % kRedPaceEvery == 0 && ch * 8 + j + 1 < D / 4)
                 __nanosleep(kRedPaceNs);
             }
           }
           if (DET) {  // one release for the warpgroup, after all of its reductions
             named_bar_sync(1, 128);
             if (et == 0) {
-              red_release_add(sem, 1);
-              if constexpr (L::kTurnRing) mbar_arrive(&bar.turn_empty[it % kTurns]);
+              if constexpr (kDual) {
+                mbar_arrive(&bar.added[it % kTurns]);  // the releaser warp releases
+              } else {
+                red_release_add(p.sem + tile_idx, 1);
+                if constexpr (L::kTurnRing) mbar_arrive(&bar.turn_empty[it % kTurns]);
+              }
             }
           }
           if (et == 0) DASH_TRACE(p, 17);
@@ -820,6 +893,7 @@ __global__ void __launch_bounds__(512, 1)
       for (int i = 0; i < kTurns; ++i) {
         mbar_init(&bar.turn_full[i], 1);
         mbar_init(&bar.turn_empty[i], 1);
+        mbar_init(&bar.added[i], 1);
       }
     }
     *s_abort = 0;
@@ -847,6 +921,9 @@ __global__ void __launch_bounds__(512, 1)
     if (warp == 1) bwd_mma<D, DET, MODE>(p, smem, tmem, bar, ab);
     if constexpr (DET) {
       if (warp == 3) bwd_sem_poller<D, DET, MODE>(p, smem, ab);
+      if constexpr (dual_of(MODE)) {
+        if (warp == 2) bwd_releaser<D, DET, MODE>(p, smem, bar, ab);
+      }
     }
   } else if (warp < 12) {
     regs_set<RegSplit<D>::kSoftmax, RegSplit<D>::kLaunch>();
@@ -895,26 +972,37 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 }  // namespace
 
-// MODE: 0 full mask, 1 causal, 2 causal with the padded (odd-N) Symmetric Shift.  The
-// parity is a constant inside the kernel, and so is the mask in the full-mask build, which
-// then carries no diagonal or schedule branches of the causal one (measured: +2 %).
+// MODE bits 0-1: 0 full mask, 1 causal, 2 causal with the padded (odd-N) Symmetric Shift;
+// bit 2: two accumulation strands (ordered, D = 128).  The parity is a constant inside the
+// kernel, and so is the mask in the full-mask build, which then carries no diagonal or
+// schedule branches of the causal one (measured: +2 %).
 template <int MODE>
 cudaError_t launch_bwd_o(int D, bool deterministic, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, int grid,
                          cudaStream_t stream) {
-  if (D == 64)
-    return deterministic ? launch_bwd_t<64, true, MODE>(tq, tk, tv, tdo, p, grid, stream)
-                         : launch_bwd_t<64, false, MODE>(tq, tk, tv, tdo, p, grid, stream);
-  return deterministic ? launch_bwd_t<128, true, MODE>(tq, tk, tv, tdo, p, grid, stream)
-                       : launch_bwd_t<128, false, MODE>(tq, tk, tv, tdo, p, grid, stream);
+  if constexpr (dual_of(MODE)) {
+    if (D != 128 || !deterministic) return cudaErrorInvalidValue;
+    return launch_bwd_t<128, true, MODE>(tq, tk, tv, tdo, p, grid, stream);
+  } else {
+    if (D == 64)
+      return deterministic ? launch_bwd_t<64, true, MODE>(tq, tk, tv, tdo, p, grid, stream)
+                           : launch_bwd_t<64, false, MODE>(tq, tk, tv, tdo, p, grid, stream);
+    return deterministic ? launch_bwd_t<128, true, MODE>(tq, tk, tv, tdo, p, grid, stream)
+                         : launch_bwd_t<128, false, MODE>(tq, tk, tv, tdo, p, grid, stream);
+  }
 }
 
 cudaError_t launch_bwd(int D, bool deterministic, int mode, const CUtensorMap &tq,
                        const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                        const BwdParams &p, int grid, cudaStream_t stream) {
-  if (mode == 2) return launch_bwd_o<2>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
-  if (mode == 1) return launch_bwd_o<1>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
-  return launch_bwd_o<0>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+  switch (mode) {
+    case 6: return launch_bwd_o<6>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+    case 5: return launch_bwd_o<5>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+    case 4: return launch_bwd_o<4>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+    case 2: return launch_bwd_o<2>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+    case 1: return launch_bwd_o<1>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+    default: return launch_bwd_o<0>(D, deterministic, tq, tk, tv, tdo, p, grid, stream);
+  }
 }
 
 }  // namespace dash

@@ -26,8 +26,8 @@ enum : uint32_t {
 struct BwdParams {
   const float *lse2;  // [B,H,N*128]  LSE * log2(e)
   const float *dvec;  // [B,H,N*128]  rowsum(dO * O)
-  float *dqacc;       // fp32 dQ accumulator, tile-native layout [B,H,N][D/4][128][4]
-  int *sem;           // [B,H,N] dQ ordering semaphores (number of partials added so far)
+  float *dqacc;       // fp32 dQ accumulator, tile-native [B,H,N][K][D/4][128][4], K strands
+  int *sem;           // [B,H,N][K] ordering semaphores (partials added so far, per strand)
   uint32_t *status;   // status word (error bit flags)
   __nv_bfloat16 *dk;  // [B,S,Hkv,D]
   __nv_bfloat16 *dv;  // [B,S,Hkv,D]
@@ -72,9 +72,9 @@ struct FwdParams {
 
 size_t fwd_smem_bytes(int D);
 
-// mode: 0 = full mask; 1 = causal mask; 2 = causal mask under Symmetric Shift (shift
-// traversal) with an odd tile count, i.e. the padded schedule.  The tile kernel is compiled
-// once per mode.
+// mode: bits 0-1: 0 = full mask; 1 = causal mask; 2 = causal mask under Symmetric Shift
+// (shift traversal) with an odd tile count, i.e. the padded schedule; bit 2 (value 4): two
+// accumulation strands (ordered, D = 128 only).  The tile kernel is compiled once per mode.
 // The ordered (deterministic) launch is cooperative: the runtime starts it only with every
 // CTA of the grid resident at once, so a worker never waits on a CTA that cannot start.
 cudaError_t launch_bwd(int D, bool deterministic, int mode, const CUtensorMap &tq,
@@ -85,7 +85,10 @@ cudaError_t launch_fwd(int D, const CUtensorMap &tq, const CUtensorMap &tk,
 cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
                               const float *lse, float *dvec, float *lse2, int B, int S, int H,
                               int D, cudaStream_t stream);
+// dQ = bf16(scale * (strand 0 + ... + strand K-1)) for every row < S.
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B,
-                              int S, int H, int D, cudaStream_t stream);
+                              int S, int H, int D, int strands, cudaStream_t stream);
+// Strands a dQ tile's accumulation is split into (DASH_SCHED_SHIFT_DUAL: 2), at most:
+constexpr int kMaxStrands = 2;
 
 }  // namespace dash

@@ -46,14 +46,23 @@ namespace dash {
 
 // kShiftFill is the packed shift schedule (below): the shift workers of all heads dealt to
 // every CTA of the grid; on the device it runs the kShift traversal with packed ranks.
-enum Sched : int { kAtomic = 0, kSerial = 1, kDescending = 2, kShift = 3, kShiftFill = 4 };
+// kShiftDual: the packed shift schedule with each dQ tile accumulated in two strands
+// (partial of rank r into strand r mod 2, in rank order; strand 0 + strand 1 at the end).
+enum Sched : int {
+  kAtomic = 0,
+  kSerial = 1,
+  kDescending = 2,
+  kShift = 3,
+  kShiftFill = 4,
+  kShiftDual = 6
+};
 
 // Which visiting order a schedule uses (ATOMIC borrows the shift order; the fill mode's
 // shift heads use the shift order).
 DASH_HD int traversal(int sched, int causal, int N) {
   (void)causal;
   (void)N;
-  if (sched == kShiftFill || sched == kAtomic) return kShift;
+  if (sched == kShiftFill || sched == kShiftDual || sched == kAtomic) return kShift;
   return sched;
 }
 

@@ -89,13 +89,21 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           partials first.  Deterministic for a given SM count (dash_sched_grid,
  *                           dash_sched_packed_rank give the order).
  *  DASH_SCHED_AUTO       -- the deterministic schedule that measured fastest on GB300 for
- *                           the mask and tile count (dash_sched_resolve names it): the pages
- *                           leave the choice to the user.  Measured over every configuration
- *                           of the benchmark (full and causal masks, D = 64 and 128,
- *                           S = 512 .. 16384, GQA 4:1, odd tile counts), SHIFT_FILL is the
- *                           fastest or within 2 % of the fastest (SERIAL at S = 512, plain
- *                           SHIFT on the GQA shape), and far ahead wherever the schedules
- *                           differ.  So AUTO = SHIFT_FILL.
+ *                           the mask, head dim, tile count and group size
+ *                           (dash_sched_resolve names it): the pages leave the choice to the
+ *                           user.  Table (from the benchmark over full and causal masks,
+ *                           D = 64 and 128, S = 512 .. 16384, GQA 4:1): full mask at D = 128
+ *                           -> SHIFT_DUAL; everything else -> SHIFT_FILL.
+ *  DASH_SCHED_SHIFT_DUAL -- packed Shift Scheduling (the SHIFT_FILL traversal, grid and ranks)
+ *                           with each dQ tile accumulated in two strands: the partial of rank
+ *                           r is added into strand r mod 2 as that strand's (r div 2)-th
+ *                           addition, each strand in order under its own semaphore, and the
+ *                           tile's dQ is bf16(scale * (strand 0 + strand 1)).  A fixed order,
+ *                           deterministic for a given SM count like SHIFT_FILL, but not the
+ *                           single chain of the pages: a strand's next contributor comes two
+ *                           lock steps later instead of one, which lets the kernel spread its
+ *                           reductions out and release each strand from a separate warp.
+ *                           D = 128 only (DASH_ERR_UNSUPPORTED at D = 64).
  */
 typedef enum {
   DASH_SCHED_ATOMIC = 0,
@@ -103,7 +111,8 @@ typedef enum {
   DASH_SCHED_DESCENDING = 2,
   DASH_SCHED_SHIFT = 3,
   DASH_SCHED_SHIFT_FILL = 4,
-  DASH_SCHED_AUTO = 5
+  DASH_SCHED_AUTO = 5,
+  DASH_SCHED_SHIFT_DUAL = 6
 } dash_sched_t;
 
 typedef enum {
@@ -129,10 +138,10 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
                             dash_mask_t mask, void *workspace, size_t workspace_bytes,
                             dash_stream_t stream);
 
-/* Bytes of device workspace dash_attn_bwd needs: a status block (256 B), the dQ ordering
- * semaphores (one per dQ tile, B*H*(Sp/128)*4), two fp32 row vectors (B*H*Sp*4 each) and the
- * fp32 dQ accumulator (B*H*Sp*D*4), Sp = 128*ceil(S/128), in this order, each part 256-byte
- * aligned; 0 on bad sizes. */
+/* Bytes of device workspace dash_attn_bwd needs, for any schedule: a status block (256 B),
+ * the dQ ordering semaphores (room for two per dQ tile, B*H*(Sp/128)*8), two fp32 row
+ * vectors (B*H*Sp*4 each) and the fp32 dQ accumulator (room for two strands, B*H*Sp*D*8),
+ * Sp = 128*ceil(S/128), in this order, each part 256-byte aligned; 0 on bad sizes. */
 size_t dash_attn_bwd_workspace_bytes(int B, int S, int H, int D);
 
 /* Backward pass (the DASH hot path): given Q, K, V, O, dO and LSE, writes dQ, dK, dV.
@@ -215,7 +224,7 @@ dash_status_t dash_attn_bwd_order_log(const void *q, const void *k, const void *
  * (no cudaMalloc/cudaFree, no allocating library routine).
  *   - Limit: sizes whose dash_attn_bwd_workspace_bytes(B,S,H,D) exceeds
  *     DASH_NOALLOC_SCRATCH_BYTES are rejected with DASH_ERR_WORKSPACE before anything runs
- *     (64 MiB holds, e.g., B*H*S*(D+2)*4 bytes for B*H*S = 126976 rows at D = 128).
+ *     (64 MiB holds about B*H*S*(2D+2)*4 bytes: up to B*H*S = 64896 rows at D = 128).
  *   - The first call on a device (that device current) looks up the array's device address
  *     with cudaGetSymbolAddress; make that first call before any stream capture.
  *   - All calls on a device share the array: calls that may overlap on the GPU (e.g. on
@@ -270,8 +279,10 @@ const char *dash_status_string(dash_status_t status);
  * Return -1 on unsupported arguments. */
 int dash_sched_workers(int sched, int mask, int N);
 /* The schedule dash_attn_bwd runs for `sched` (DASH_SCHED_AUTO resolved, every other value
- * returned unchanged) with `mask` and N = ceil(S/128) tiles; -1 on bad arguments. */
-int dash_sched_resolve(int sched, int mask, int N);
+ * returned unchanged) with `mask`, head dim D, N = ceil(S/128) tiles and `group` query heads
+ * per KV head; -1 on bad arguments.  The table queries below resolve AUTO to SHIFT_FILL,
+ * whose traversal SHIFT_DUAL shares. */
+int dash_sched_resolve(int sched, int mask, int D, int N, int group);
 /* Number of CTAs dash_attn_bwd launches for its tile kernel on a GPU with `sms` SMs, for
  * `heads` = B * H/group (batch, kv head) pairs; -1 where dash_attn_bwd would reject the
  * schedule arguments (e.g. DASH_SCHED_SHIFT with more workers per head than SMs). */

@@ -35,12 +35,12 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_workspace_sizes(L):
-    """Status block, one semaphore per dQ tile, two row vectors and the fp32 accumulator,
-    each part 256-byte aligned."""
+    """Status block, room for two semaphores per dQ tile, two row vectors and a two-strand
+    fp32 accumulator, each part 256-byte aligned."""
     B, S, H, D = 2, 1024, 4, 128
     n = dash.bwd_workspace_bytes(B, S, H, D)
     rows = B * H * S
-    need = 256 + B * H * (S // 128) * 4 + 2 * rows * 4 + rows * D * 4
+    need = 256 + 2 * B * H * (S // 128) * 4 + 2 * rows * 4 + 2 * rows * D * 4
     assert need <= n < need + 4 * 256
     # a partial last tile is padded to whole tiles: S = 1000 needs the space of S = 1024
     assert dash.bwd_workspace_bytes(B, 1000, H, D) == dash.bwd_workspace_bytes(B, 1024, H, D)
@@ -60,7 +60,7 @@ def test_argument_errors_are_synchronous(L):
                         1, 512, 3, 2, 64, 0.0, 0, 1, null, 0, null)
     assert c == 1                                                # H % group
     fake = 1 << 20                                               # never dereferenced
-    c = L.dash_attn_bwd(*([fake] * 9), 1, 384, 2, 1, 64, 0.0, 1, 6, fake, 1 << 30, null)
+    c = L.dash_attn_bwd(*([fake] * 9), 1, 384, 2, 1, 64, 0.0, 1, 7, fake, 1 << 30, null)
     assert c == 1                                                # unknown schedule
     c = L.dash_attn_bwd_stages(*([fake] * 9), 1, 384, 2, 1, 64, 0.0, 1, 1, fake, 1 << 30, 8,
                                null)
@@ -77,7 +77,7 @@ def test_argument_errors_are_synchronous(L):
 
 
 SCHEDS = [("serial", sc.SERIAL), ("descending", sc.DESCENDING), ("atomic", None),
-          ("shift", None), ("shift_fill", None)]
+          ("shift", None), ("shift_fill", None), ("shift_dual", None)]
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 33, 64, 127, 128])
@@ -132,8 +132,8 @@ def test_packed_ranks_equal_oracle(L, causal, N, heads, P):
 def test_grid_sizes(L, causal):
     N, heads, sms = 32, 64, 152
     W = N // 2 if causal else N
-    for name in ("serial", "descending", "shift", "shift_fill", "atomic"):
-        w = W if name in ("shift", "shift_fill", "atomic") else N
+    for name in ("serial", "descending", "shift", "shift_fill", "shift_dual", "atomic"):
+        w = W if name in ("shift", "shift_fill", "shift_dual", "atomic") else N
         assert dash.sched_grid(name, causal, N, heads, sms) == min(heads * w, sms)
     assert dash.sched_grid("shift_fill", causal, N, 1, sms) == W
     with pytest.raises(ValueError):
@@ -151,18 +151,23 @@ def test_schedule_query_rejects_bad_arguments(L):
     assert L.dash_sched_step(1, 0, 4, 0, 0, 4, None, None, None) == -1
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_auto_schedule_resolution(L, causal, N):
-    """AUTO runs the packed shift schedule for every mask and tile count; other schedules
-    pass through."""
-    want = "shift_fill"
-    assert dash.sched_resolve("auto", causal, N) == want
-    for name in ("atomic", "serial", "descending"):
-        assert dash.sched_resolve(name, causal, N) == name
-    assert dash.sched_table("auto", causal, N) == dash.sched_table(want, causal, N)
+def test_auto_schedule_resolution(L, causal, N, D):
+    """AUTO runs the measured table's schedule: the two-strand packed shift for the full mask
+    at D = 128, the packed shift otherwise; other schedules pass through, and the table
+    queries (which do not know D) see the packed shift traversal both share."""
+    want = "shift_dual" if (D == 128 and not causal) else "shift_fill"
+    assert dash.sched_resolve("auto", causal, N, D) == want
+    assert dash.sched_resolve("auto", causal, N, D, group=4) == want
+    for name in ("atomic", "serial", "descending", "shift", "shift_fill", "shift_dual"):
+        assert dash.sched_resolve(name, causal, N, D) == name
+    assert dash.sched_table("auto", causal, N) == dash.sched_table("shift_fill", causal, N)
+    assert dash.sched_table("shift_dual", causal, N) == dash.sched_table("shift_fill", causal, N)
     assert dash.sched_grid("auto", causal, N, 64, 152) == dash.sched_grid(want, causal, N, 64, 152)
-    assert L.dash_sched_resolve(6, int(causal), N) == -1
+    assert L.dash_sched_resolve(7, int(causal), D, N, 1) == -1
+    assert L.dash_sched_resolve(5, int(causal), 96, N, 1) == -1
 
 
 def test_varlen_arguments_and_workspace(L):
@@ -181,7 +186,7 @@ def test_varlen_arguments_and_workspace(L):
                                   None) == 1
     assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 3, 64, 0.0, 0, 1, fake, 1 << 30, None) == 1
     assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 1, 64, 0.0, 0, 9, fake, 1 << 30, None) == 1
-    assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 1, 64, 0.0, 0, 6, fake, 1 << 30, None) == 1
+    assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 1, 64, 0.0, 0, 7, fake, 1 << 30, None) == 1
     assert L.dash_attn_fwd_varlen(*([fake] * 5), arr([2, 4]), 1, 4, 1, 64, 0.0, 0, fake, 256,
                                   None) == 1
 

@@ -1,8 +1,9 @@
 """Determinism of the ordered schedules on the GPU, as the target states it: 100 repeated
 runs of every deterministic schedule give bit-identical dQ, dK, dV, idle and while other
 kernels load the GPU from a second stream, at both head dims and at 128 tiles per head;
-after a run every dQ tile's ordering semaphore holds exactly the number of partials the tile
-received (every partial went through its turn, none was skipped or added twice); and the
+after a run every dQ tile's ordering semaphore (each strand's, for the two-strand schedule)
+holds exactly the number of partials it received (every partial went through its turn, none
+was skipped or added twice); and the
 ordered tile kernel starts only once all of its CTAs can be resident,
 so SMs held by another kernel delay it instead of leaving its workers waiting on CTAs that
 cannot start."""
@@ -16,7 +17,12 @@ from dash_inputs import make_qkv_do
 
 pytestmark = pytest.mark.gpu
 
-DETERMINISTIC = ["serial", "descending", "shift", "shift_fill"]
+DETERMINISTIC = ["serial", "descending", "shift", "shift_fill", "shift_dual"]
+
+
+def scheds_for(D):
+    """The ordered schedules a head dim runs (the two-strand kernel is D = 128 only)."""
+    return [s for s in DETERMINISTIC if D == 128 or s != "shift_dual"]
 REPEATS = 100
 SHAPES = [(2, 2048, 4, 2, 128), (1, 1024, 2, 2, 64)]
 
@@ -43,12 +49,12 @@ class Problem:
                       schedule=sched, dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws)
         return self.dq, self.dk, self.dv
 
-    def semaphores(self):
-        """The [B, H, N] semaphores of the workspace (layout: 256-byte status block, then
-        one int32 per dQ tile)."""
+    def semaphores(self, K):
+        """The semaphores of the workspace (layout: 256-byte status block, then one int32 per
+        dQ tile and strand, [B, H, N][K] for a call with K strands)."""
         B, S, H, _, D = self.shape
         N = S // 128
-        return self.ws[256:256 + 4 * B * H * N].view(torch.int32).view(B, H, N)
+        return self.ws[256:256 + 4 * B * H * N * K].view(torch.int32).view(B, H, N, K)
 
 
 def snapshot(outs):
@@ -59,7 +65,7 @@ def snapshot(outs):
 @pytest.mark.parametrize("shape", SHAPES, ids=["d128", "d64"])
 def test_hundred_repeats_bit_identical(dash, shape, causal):
     p = Problem(dash, *shape, causal, seed=1)
-    for sched in DETERMINISTIC:
+    for sched in scheds_for(shape[4]):
         ref = snapshot(p.run(sched))
         for _ in range(REPEATS):
             out = p.run(sched)
@@ -73,7 +79,7 @@ def test_hundred_repeats_at_128_tiles(dash, causal):
     """S = 16384 (N = 128 tiles, the longest sequence of the benchmark), four heads: the
     packed schedules split heads across rounds of the grid here."""
     p = Problem(dash, 1, 16384, 4, 4, 128, causal, seed=6)
-    for sched in DETERMINISTIC:
+    for sched in scheds_for(128):
         ref = snapshot(p.run(sched))
         for _ in range(REPEATS):
             out = p.run(sched)
@@ -92,7 +98,7 @@ def test_bit_identical_under_concurrent_load(dash, shape, causal):
     side = torch.cuda.Stream()
     a = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
     sink = torch.empty_like(a)
-    for sched in DETERMINISTIC:
+    for sched in scheds_for(shape[4]):
         torch.cuda.synchronize()
         ref = snapshot(p.run(sched))
         torch.cuda.synchronize()
@@ -112,19 +118,21 @@ def test_bit_identical_under_concurrent_load(dash, shape, causal):
 def test_every_partial_takes_its_turn(dash, shape, causal):
     p = Problem(dash, *shape, causal, seed=0)
     N = shape[1] // 128
-    want = np.array([(q + 1) if causal else N for q in range(N)], dtype=np.int32)
-    for sched in DETERMINISTIC:
+    n = np.array([(q + 1) if causal else N for q in range(N)])
+    for sched in scheds_for(shape[4]):
+        K = dash.STRANDS[sched]
+        want = np.stack([np.where(n > s, (n - s + K - 1) // K, 0) for s in range(K)], axis=-1)
         p.run(sched)
         p.dash.status(p.ws)
-        sem = p.semaphores().cpu().numpy()
-        assert (sem == want[None, None, :]).all(), sched
+        sem = p.semaphores(K).cpu().numpy()
+        assert (sem == want[None, None].astype(np.int32)).all(), sched
 
 
 @pytest.mark.parametrize("shape,causal", [((2, 1024, 4, 2, 128), False), ((2, 1024, 4, 2, 128), True),
                                           ((1, 384, 2, 2, 64), True)])
 def test_auto_runs_the_resolved_schedule(dash, shape, causal):
     p = Problem(dash, *shape, causal, seed=3)
-    want = dash.sched_resolve("auto", causal, shape[1] // 128)
+    want = dash.sched_resolve("auto", causal, shape[1] // 128, shape[4], shape[2] // shape[3])
     ref = snapshot(p.run(want))
     out = p.run("auto")
     p.dash.status(p.ws)
@@ -132,7 +140,7 @@ def test_auto_runs_the_resolved_schedule(dash, shape, causal):
         assert torch.equal(a, b), want
 
 
-@pytest.mark.parametrize("sched", ["shift_fill", "serial"])
+@pytest.mark.parametrize("sched", ["shift_fill", "shift_dual", "serial"])
 def test_waits_for_sms_held_by_another_kernel(dash, sched):
     """Kernels on other streams hold some SMs for 0.5 s while the device-side wait limit is
     0.2 s.  A grid started with only part of its CTAs resident would leave its first

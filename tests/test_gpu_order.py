@@ -14,7 +14,7 @@ from oracle import schedule as sc
 
 pytestmark = pytest.mark.gpu
 
-ORDERED = ["serial", "descending", "shift", "shift_fill"]
+ORDERED = ["serial", "descending", "shift", "shift_fill", "shift_dual"]
 
 
 @pytest.fixture(scope="module")
@@ -29,6 +29,8 @@ def oracle_ranks(dash, sched, causal, B, H, Hkv, N):
     """[B, H, N, N] rank of (q, kv) in tile q's order per the oracle; -1 where skipped."""
     G = H // Hkv
     want = np.full((B, H, N, N), -1, dtype=np.int32)
+    if sched == "shift_dual":  # the packed shift's ranks, split into strands by parity
+        sched = "shift_fill"
     if sched in ("serial", "descending"):
         for q in range(N):
             for kv in range(N):
@@ -52,6 +54,9 @@ def oracle_ranks(dash, sched, causal, B, H, Hkv, N):
 
 ORDER_CASES = [  # (B, S, H, Hkv, D, causal)
     (1, 1024, 2, 2, 64, False),     # N = 8
+    (1, 1024, 2, 2, 128, False),
+    (2, 4096, 16, 16, 128, True),   # 32 heads of 16 pairs: heads split across rounds
+    (1, 16384, 2, 2, 128, False),
     (1, 640, 2, 2, 128, True),      # odd N = 5: padded Symmetric Shift
     (2, 1024, 8, 2, 128, True),     # GQA 4:1
     (4, 4096, 32, 32, 64, True),    # 128 heads of 16 pairs: heads split across rounds
@@ -66,6 +71,8 @@ ORDER_CASES = [  # (B, S, H, Hkv, D, causal)
 def test_executed_order_equals_oracle(dash, sched, case):
     B, S, H, Hkv, D, causal = case
     N = (S + 127) // 128
+    if sched == "shift_dual" and D != 128:
+        pytest.skip("the two-strand kernel is D = 128 only")
     if sched == "shift" and dash.sched_grid("shift_fill", causal, N, 1, 10 ** 6) > \
             torch.cuda.get_device_properties(0).multi_processor_count:
         pytest.skip("plain SHIFT needs a head's workers resident at once")
