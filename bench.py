@@ -39,28 +39,33 @@ WORKLOADS = {
         desc="full-mask attention backward, H=16, D=128, bf16 N(0,1), B*S=16384, "
              "S swept over {512,1024,2048,4096,8192,16384}",
         H=16, Hkv=16, D=128, causal=False, tokens=16384,
-        seqs=[512, 1024, 2048, 4096, 8192, 16384], schedule="shift_fill", ref_S=2048),
+        seqs=[512, 1024, 2048, 4096, 8192, 16384], schedule="auto", ref_S=2048),
     "causal_h32_d128": dict(
         desc="causal-mask attention backward, H=32, D=128, bf16 N(0,1), B*S=16384, "
              "S swept over {1024,2048,4096,8192,16384}",
         H=32, Hkv=32, D=128, causal=True, tokens=16384,
-        seqs=[1024, 2048, 4096, 8192, 16384], schedule="shift_fill", ref_S=2048),
+        seqs=[1024, 2048, 4096, 8192, 16384], schedule="auto", ref_S=2048),
     "causal_h32_d64": dict(
         desc="causal-mask attention backward, H=32, D=64, bf16 N(0,1), B*S=16384, "
              "S swept over {1024,4096,16384}",
         H=32, Hkv=32, D=64, causal=True, tokens=16384, seqs=[1024, 4096, 16384],
-        schedule="shift_fill", ref_S=2048),
+        schedule="auto", ref_S=2048),
     "gqa_causal_8b": dict(
         desc="GQA causal attention backward shaped like an 8B decoder layer: 32 query heads, "
              "8 KV heads, D=128, B=2, S=8192",
-        H=32, Hkv=8, D=128, causal=True, tokens=16384, seqs=[8192], schedule="shift_fill",
+        H=32, Hkv=8, D=128, causal=True, tokens=16384, seqs=[8192], schedule="auto",
         ref_S=2048),
     "small_b1_h2_s512_d64": dict(
         desc="full-mask attention backward, B=1, H=2, S=512, D=64 (4 KV blocks)",
-        H=2, Hkv=2, D=64, causal=False, tokens=512, seqs=[512], schedule="shift_fill", ref_S=512),
+        H=2, Hkv=2, D=64, causal=False, tokens=512, seqs=[512], schedule="auto", ref_S=512),
 }
 SCHEDULES = ["atomic", "serial", "descending", "shift", "shift_fill", "shift_dual"]
 DETERMINISTIC = ["serial", "descending", "shift", "shift_fill", "shift_dual"]
+
+
+def schedules_for(D):
+    """Schedules a head dim runs (the two-strand kernel is D = 128 only)."""
+    return [s for s in SCHEDULES if D == 128 or s != "shift_dual"]
 FALLBACK_PEAK_TFLOPS = 1900.0   # only if the measured-peaks file is absent
 PROFILE = os.path.join(ROOT, "profiles", "bwd_tile_kernel_full_h16_d128.md")
 KERNEL_SOURCES = ["bwd.cu", "ptx.cuh", "sched.cuh", "common.cuh"]
@@ -253,9 +258,10 @@ def run_gpu(args, wl, rank, world):
 
     # per-schedule comparison (interleaved, median of reps) on the same inputs
     reps = max(3, min(10, args.steps))
-    per = {s: [[] for _ in probs] for s in SCHEDULES}
+    scheds = schedules_for(D)
+    per = {s: [[] for _ in probs] for s in scheds}
     for _ in range(reps):
-        for s in SCHEDULES:
+        for s in scheds:
             for j, p in enumerate(probs):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
@@ -264,17 +270,24 @@ def run_gpu(args, wl, rank, world):
                 per[s][j].append((a, b))
     torch.cuda.synchronize()
     sweep = []
-    tot = {s: 0.0 for s in SCHEDULES}
+    tot = {s: 0.0 for s in scheds}
     for j, p in enumerate(probs):
         row = {"S": p["S"], "B": p["B"]}
-        for s in SCHEDULES:
+        for s in scheds:
             ms = statistics.median(a.elapsed_time(b) for a, b in per[s][j])
             tot[s] += ms
             row[s + "_tflops"] = round(p["flops"] / ms / 1e9, 1)
         for s in DETERMINISTIC:
-            row[s + "_slowdown_vs_atomic"] = round(row["atomic_tflops"] / row[s + "_tflops"] - 1, 4)
+            if s in scheds:
+                row[s + "_slowdown_vs_atomic"] = round(row["atomic_tflops"] / row[s + "_tflops"] - 1, 4)
+        row["auto_runs"] = dash.sched_resolve("auto", causal, (p["S"] + 127) // 128, D, H // Hkv)
         sweep.append(row)
-    sched_summary = {s: round(step_flops / tot[s] / 1e9, 1) for s in SCHEDULES}
+    sched_summary = {s: round(step_flops / tot[s] / 1e9, 1) for s in scheds}
+    # the schedule the timed step ran at each point (AUTO resolved)
+    ran = [dash.sched_resolve(sched, causal, (p["S"] + 127) // 128, D, H // Hkv) for p in probs]
+    ran_ms = sum(statistics.median(a.elapsed_time(b) for a, b in per[r][j])
+                 for j, r in enumerate(ran))
+    ran_tflops = step_flops / ran_ms / 1e9
 
     # end to end through the public API with host buffers (pinned), copies in the region
     e2e_val, h2d, d2h = None, 0, 0
@@ -333,6 +346,9 @@ def run_gpu(args, wl, rank, world):
         torch.cuda.synchronize()
         e2e_val = step_flops * n_e2e / (a.elapsed_time(b) / 1e3) / 1e12 * world
 
+    configs = None if (args.no_configs or args.quick) else other_configs(args, dev, dash)
+    block = None if (args.no_block or args.quick) else block_timing()
+
     peak, peak_sus, peak_kind = peaks()
     value = job_tflops(step_flops, args.steps, world, elapsed_ms)
     tile_tflops = step_flops * args.steps / (tile_ms / 1e3) / 1e12
@@ -349,13 +365,14 @@ def run_gpu(args, wl, rank, world):
                          "inputs smaller than L2; no flush (parity-size workload)",
                    "step": "prologue + tile kernel + dQ convert for every S of the sweep"},
         "pct_of_peak": round(100 * value / world / peak, 2),
-        "slowdown_vs_atomic": round(sched_summary["atomic"] / sched_summary[sched] - 1, 4),
+        "slowdown_vs_atomic": round(sched_summary["atomic"] / ran_tflops - 1, 4),
+        "schedule_ran": sorted(set(ran)),
         "schedules_tflops": sched_summary,
         "sweep": sweep,
         "roofline": {"bound": "tensor", "achieved": round(tile_tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tile_tflops / peak, 4),
                      "traffic": profiled_traffic(args.workload),
-                     "kernel": "bwd_kernel (tile kernel, " + sched + ")",
+                     "kernel": "bwd_kernel (tile kernel, " + sched + " -> " + "/".join(sorted(set(ran))) + ")",
                      "peak_source": f"{peak_kind} dense bf16 burst"
                                     + (f"; sustained {peak_sus}" if peak_sus else "")},
         "e2e": {"value": round(e2e_val, 2) if e2e_val else None, "unit": "TFLOP/s",
@@ -363,7 +380,79 @@ def run_gpu(args, wl, rank, world):
         "clocks": clk.summary(),
         "gpu_launches": 3 * len(probs) * args.steps,
     }
+    if configs is not None:
+        res["configs"] = configs
+    if block is not None:
+        res["block"] = block
     return res
+
+
+def other_configs(args, dev, dash):
+    """Every other workload of the benchmark, each sequence length timed for every schedule
+    (whole backward call, interleaved, median of 3 after a warm-up), with the best
+    deterministic schedule and its slowdown against the atomic variant.  Inputs are seeded
+    N(0,1) draws made on the device (torch's CUDA generator), O and LSE from the forward."""
+    import torch
+    peak = peaks()[0]
+    out = {}
+    for name, wl in WORKLOADS.items():
+        if name == args.workload:
+            continue
+        H, Hkv, D, causal = wl["H"], wl["Hkv"], wl["D"], wl["causal"]
+        scheds = schedules_for(D)
+        rows = []
+        for S in wl["seqs"]:
+            B = max(1, wl["tokens"] // S)
+            g = torch.Generator(device=dev).manual_seed(0)
+            q = torch.randn(B, S, H, D, device=dev, generator=g).to(torch.bfloat16)
+            k = torch.randn(B, S, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
+            v = torch.randn(B, S, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
+            do = torch.randn(B, S, H, D, device=dev, generator=g).to(torch.bfloat16)
+            o, lse = dash.fwd(q, k, v, causal=causal, check=True)
+            ws = torch.empty(dash.bwd_workspace_bytes(B, S, H, D), dtype=torch.uint8, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            flops = bwd_flops(B, S, H, D, causal)
+
+            def call(s):
+                dash.bwd(q, k, v, o, do, lse, causal=causal, schedule=s, dq=dq, dk=dk, dv=dv,
+                         workspace=ws)
+            for s in scheds:
+                call(s)
+            dash.status(ws)
+            ev = {s: [] for s in scheds}
+            for _ in range(3):
+                for s in scheds:
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    call(s)
+                    b.record()
+                    ev[s].append((a, b))
+            torch.cuda.synchronize()
+            dash.status(ws)
+            row = {"S": S, "B": B}
+            for s in scheds:
+                row[s + "_tflops"] = round(flops / statistics.median(a.elapsed_time(b) for a, b in ev[s]) / 1e9, 1)
+            best = max(DETERMINISTIC if D == 128 else [x for x in DETERMINISTIC if x != "shift_dual"],
+                       key=lambda x: row[x + "_tflops"])
+            auto = dash.sched_resolve("auto", causal, (S + 127) // 128, D, H // Hkv)
+            row.update({"best_deterministic": best,
+                        "best_slowdown_vs_atomic": round(row["atomic_tflops"] / row[best + "_tflops"] - 1, 4),
+                        "best_pct_of_peak": round(100 * row[best + "_tflops"] / peak, 2),
+                        "auto_runs": auto,
+                        "auto_slowdown_vs_atomic": round(row["atomic_tflops"] / row[auto + "_tflops"] - 1, 4)})
+            rows.append(row)
+            del q, k, v, do, o, lse, ws, dq, dk, dv
+            torch.cuda.empty_cache()
+        out[name] = {"description": wl["desc"], "points": rows}
+    return out
+
+
+def block_timing():
+    """Forward + backward of the synthetic 8B-shaped decoder block (random weights) with the
+    library's attention under the atomic, serialized and AUTO schedules."""
+    from deterministic_attention_backward_gb300.block import time_block
+    return time_block(seq=8192, batch=1, schedules=("atomic", "serial", "shift_fill", "auto"),
+                      steps=5, warmup=3)
 
 
 # ------------------------------------------------------------------------------ CPU oracle
@@ -438,10 +527,14 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="full_h16_d128", choices=sorted(WORKLOADS))
-    ap.add_argument("--schedule", default=None, choices=SCHEDULES)
+    ap.add_argument("--schedule", default=None, choices=SCHEDULES + ["auto"])
     ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-schedule table of the other workloads")
+    ap.add_argument("--no-block", action="store_true",
+                    help="skip the transformer-block timing")
     ap.add_argument("--seq", type=int, default=0,
                     help="run one sequence length of the workload's sweep only")
     ap.add_argument("--quick", action="store_true",

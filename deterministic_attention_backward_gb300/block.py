@@ -59,6 +59,9 @@ class Block:
         self.n1 = torch.ones(hidden, device=device, dtype=torch.bfloat16, requires_grad=True)
         self.n2 = torch.ones(hidden, device=device, dtype=torch.bfloat16, requires_grad=True)
         self.attn = _attention_function()
+        # when a dict: the attention's inputs and output of the last call are kept there, with
+        # their gradients retained (q/k/v.grad = dQ/dK/dV, o.grad = the upstream dO)
+        self.capture = None
 
     @staticmethod
     def _rms(x, weight):
@@ -73,7 +76,12 @@ class Block:
         q = q.reshape(B, S, self.h, self.d).contiguous()
         k = k.reshape(B, S, self.hk, self.d).contiguous()
         v = v.reshape(B, S, self.hk, self.d).contiguous()
-        a = self.attn.apply(q, k, v, causal, schedule).reshape(B, S, self.h * self.d)
+        o = self.attn.apply(q, k, v, causal, schedule)
+        if self.capture is not None:
+            for t in (q, k, v, o):
+                t.retain_grad()
+            self.capture.update(q=q, k=k, v=v, o=o)
+        a = o.reshape(B, S, self.h * self.d)
         x = x + a @ self.wo
         hid = self._rms(x, self.n2)
         import torch.nn.functional as F
@@ -83,8 +91,8 @@ class Block:
         return [self.wqkv, self.wo, self.w1, self.w3, self.w2, self.n1, self.n2]
 
 
-def time_block(seq=8192, batch=1, schedules=("atomic", "serial", "shift_fill"), steps=10,
-               warmup=3, causal=True, seed=0):
+def time_block(seq=8192, batch=1, schedules=("atomic", "serial", "shift_fill", "auto"),
+               steps=10, warmup=3, causal=True, seed=0):
     """Median forward+backward time (ms) of one block per schedule, and each
     deterministic schedule's slowdown against ``atomic``."""
     import torch

@@ -143,14 +143,14 @@ bool sched_known(int sched) {
 }
 
 // DASH_SCHED_AUTO: the deterministic schedule measured fastest on GB300 for the mask, head
-// dim D, tile count N and group size G (the table is in the header).  D = 0 asks for the
-// traversal only (the schedule queries): SHIFT_FILL, whose tables DASH_SCHED_SHIFT_DUAL
-// shares.
+// dim D, tile count N and group size G (the table and its measurements are in the header).
+// D = 0 asks for the traversal only (the schedule queries): SHIFT_FILL, whose tables
+// DASH_SCHED_SHIFT_DUAL shares.
 int resolve_sched(int sched, int mask, int D, int N, int G) {
-  (void)N;
-  (void)G;
   if (sched != DASH_SCHED_AUTO) return sched;
-  return (D == 128 && mask == DASH_MASK_FULL) ? DASH_SCHED_SHIFT_DUAL : DASH_SCHED_SHIFT_FILL;
+  if (D != 128 || N < 8) return DASH_SCHED_SHIFT_FILL;
+  if (mask == DASH_MASK_FULL || G > 1 || N >= 64) return DASH_SCHED_SHIFT_DUAL;
+  return DASH_SCHED_SHIFT_FILL;
 }
 
 // False when plain SHIFT cannot have every worker of a head resident at once.  The packed

@@ -89,11 +89,16 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           partials first.  Deterministic for a given SM count (dash_sched_grid,
  *                           dash_sched_packed_rank give the order).
  *  DASH_SCHED_AUTO       -- the deterministic schedule that measured fastest on GB300 for
- *                           the mask, head dim, tile count and group size
+ *                           the mask, head dim, tile count N and group size G
  *                           (dash_sched_resolve names it): the pages leave the choice to the
- *                           user.  Table (from the benchmark over full and causal masks,
- *                           D = 64 and 128, S = 512 .. 16384, GQA 4:1): full mask at D = 128
- *                           -> SHIFT_DUAL; everything else -> SHIFT_FILL.
+ *                           user.  Table, from the benchmark's whole-call timings (full mask
+ *                           H16 and causal H32 at D = 128 and 64, S = 512 .. 16384, GQA 4:1):
+ *                             D = 64, or N < 8                    -> SHIFT_FILL
+ *                             D = 128, full mask                  -> SHIFT_DUAL (+5 % at
+ *                                                                    N = 8, +16 % at N = 128)
+ *                             D = 128, causal, G > 1              -> SHIFT_DUAL (+8 %, N = 64)
+ *                             D = 128, causal, G = 1, N >= 64     -> SHIFT_DUAL (+0.5-3 %)
+ *                             D = 128, causal, G = 1, N < 64      -> SHIFT_FILL (2-8 % ahead)
  *  DASH_SCHED_SHIFT_DUAL -- packed Shift Scheduling (the SHIFT_FILL traversal, grid and ranks)
  *                           with each dQ tile accumulated in two strands: the partial of rank
  *                           r is added into strand r mod 2 as that strand's (r div 2)-th

@@ -151,21 +151,30 @@ def test_schedule_query_rejects_bad_arguments(L):
     assert L.dash_sched_step(1, 0, 4, 0, 0, 4, None, None, None) == -1
 
 
+def auto_table(causal, D, N, G):
+    """The measured table the header documents for DASH_SCHED_AUTO."""
+    if D != 128 or N < 8:
+        return "shift_fill"
+    if not causal or G > 1 or N >= 64:
+        return "shift_dual"
+    return "shift_fill"
+
+
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8, 128])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8, 16, 63, 64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_auto_schedule_resolution(L, causal, N, D):
-    """AUTO runs the measured table's schedule: the two-strand packed shift for the full mask
-    at D = 128, the packed shift otherwise; other schedules pass through, and the table
-    queries (which do not know D) see the packed shift traversal both share."""
-    want = "shift_dual" if (D == 128 and not causal) else "shift_fill"
-    assert dash.sched_resolve("auto", causal, N, D) == want
-    assert dash.sched_resolve("auto", causal, N, D, group=4) == want
+    """AUTO runs the measured table's schedule; other schedules pass through, and the table
+    queries (which do not know D) see the packed shift traversal both packed schedules
+    share."""
+    for G in (1, 4):
+        want = auto_table(causal, D, N, G)
+        assert dash.sched_resolve("auto", causal, N, D, group=G) == want
+        assert dash.sched_grid("auto", causal, N, 64, 152) == dash.sched_grid(want, causal, N, 64, 152)
     for name in ("atomic", "serial", "descending", "shift", "shift_fill", "shift_dual"):
         assert dash.sched_resolve(name, causal, N, D) == name
     assert dash.sched_table("auto", causal, N) == dash.sched_table("shift_fill", causal, N)
     assert dash.sched_table("shift_dual", causal, N) == dash.sched_table("shift_fill", causal, N)
-    assert dash.sched_grid("auto", causal, N, 64, 152) == dash.sched_grid(want, causal, N, 64, 152)
     assert L.dash_sched_resolve(7, int(causal), D, N, 1) == -1
     assert L.dash_sched_resolve(5, int(causal), 96, N, 1) == -1
 

@@ -128,8 +128,12 @@ def test_every_partial_takes_its_turn(dash, shape, causal):
         assert (sem == want[None, None].astype(np.int32)).all(), sched
 
 
-@pytest.mark.parametrize("shape,causal", [((2, 1024, 4, 2, 128), False), ((2, 1024, 4, 2, 128), True),
-                                          ((1, 384, 2, 2, 64), True)])
+@pytest.mark.parametrize("shape,causal", [
+    ((2, 1024, 4, 2, 128), False), ((2, 1024, 4, 2, 128), True), ((1, 384, 2, 2, 64), True),
+    # the benchmark's configurations at their largest point (full H16 D128 S16k, causal H32
+    # D128 S16k, causal H32 D64 S16k, GQA 32/8 D128 B2 S8192, B1 H2 S512 D64)
+    ((1, 16384, 16, 16, 128), False), ((1, 16384, 32, 32, 128), True),
+    ((1, 16384, 32, 32, 64), True), ((2, 8192, 32, 8, 128), True), ((1, 512, 2, 2, 64), False)])
 def test_auto_runs_the_resolved_schedule(dash, shape, causal):
     p = Problem(dash, *shape, causal, seed=3)
     want = dash.sched_resolve("auto", causal, shape[1] // 128, shape[4], shape[2] // shape[3])
