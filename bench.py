@@ -64,8 +64,8 @@ DETERMINISTIC = ["serial", "descending", "shift", "shift_fill", "shift_dual"]
 
 
 def schedules_for(D):
-    """Schedules a head dim runs (the two-strand kernel is D = 128 only)."""
-    return [s for s in SCHEDULES if D == 128 or s != "shift_dual"]
+    """Schedules a head dim runs (all of them)."""
+    return list(SCHEDULES)
 FALLBACK_PEAK_TFLOPS = 1900.0   # only if the measured-peaks file is absent
 PROFILE = os.path.join(ROOT, "profiles", "bwd_tile_kernel_full_h16_d128.md")
 KERNEL_SOURCES = ["bwd.cu", "ptx.cuh", "sched.cuh", "common.cuh"]
@@ -95,15 +95,16 @@ def kernel_source_hash():
 
 
 def profiled_traffic(workload):
-    """dram bytes per tile-kernel launch from the committed ncu summary, if it was taken
-    on the current kernel source and this workload; else None."""
+    """dram bytes per tile-kernel launch, cached from the committed ncu summary (ncu cannot
+    run inside the timed bench), if it was taken on the current kernel source and this
+    workload; else None."""
     try:
         text = open(PROFILE).read()
     except OSError:
         return None
     src = re.search(r"kernel source sha256\[:16\]:\s*([0-9a-f]+)", text)
     wl = re.search(r"workload:\s*(\S+)", text)
-    tr = re.search(r"dram bytes per launch \(scaled to the bench launch mix\):\s*([0-9.eE+]+)", text)
+    tr = re.search(r"dram bytes per launch[^:]*:\s*([0-9.eE+]+)", text)
     if not (src and wl and tr) or src.group(1) != kernel_source_hash() or wl.group(1) != workload:
         return None
     return float(tr.group(1))
@@ -372,6 +373,10 @@ def run_gpu(args, wl, rank, world):
         "roofline": {"bound": "tensor", "achieved": round(tile_tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tile_tflops / peak, 4),
                      "traffic": profiled_traffic(args.workload),
+                     "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of one "
+                                       "S=4096 tile-kernel launch, cached from "
+                                       "profiles/bwd_tile_kernel_full_h16_d128.md (null when "
+                                       "the kernel source changed since the capture)",
                      "kernel": "bwd_kernel (tile kernel, " + sched + " -> " + "/".join(sorted(set(ran))) + ")",
                      "peak_source": f"{peak_kind} dense bf16 burst"
                                     + (f"; sustained {peak_sus}" if peak_sus else "")},
@@ -432,8 +437,7 @@ def other_configs(args, dev, dash):
             row = {"S": S, "B": B}
             for s in scheds:
                 row[s + "_tflops"] = round(flops / statistics.median(a.elapsed_time(b) for a, b in ev[s]) / 1e9, 1)
-            best = max(DETERMINISTIC if D == 128 else [x for x in DETERMINISTIC if x != "shift_dual"],
-                       key=lambda x: row[x + "_tflops"])
+            best = max(DETERMINISTIC, key=lambda x: row[x + "_tflops"])
             auto = dash.sched_resolve("auto", causal, (S + 127) // 128, D, H // Hkv)
             row.update({"best_deterministic": best,
                         "best_slowdown_vs_atomic": round(row["atomic_tflops"] / row[best + "_tflops"] - 1, 4),

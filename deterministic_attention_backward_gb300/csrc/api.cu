@@ -148,8 +148,9 @@ bool sched_known(int sched) {
 // DASH_SCHED_SHIFT_DUAL shares.
 int resolve_sched(int sched, int mask, int D, int N, int G) {
   if (sched != DASH_SCHED_AUTO) return sched;
-  if (D != 128 || N < 8) return DASH_SCHED_SHIFT_FILL;
-  if (mask == DASH_MASK_FULL || G > 1 || N >= 64) return DASH_SCHED_SHIFT_DUAL;
+  if (N < 8) return DASH_SCHED_SHIFT_FILL;
+  if (mask == DASH_MASK_FULL) return DASH_SCHED_SHIFT_DUAL;
+  if (D == 128 && (G > 1 || N >= 64)) return DASH_SCHED_SHIFT_DUAL;
   return DASH_SCHED_SHIFT_FILL;
 }
 
@@ -262,7 +263,6 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   if (!make_plan(sched, causal, N, B * Hkv, dev.sms, &plan)) return DASH_ERR_UNSUPPORTED;
   const bool ordered = sched != DASH_SCHED_ATOMIC;
   const int K = plan.strands;
-  if (K > 1 && D != 128) return DASH_ERR_UNSUPPORTED;  // the two-strand kernel is D = 128
 
   CUtensorMap tq, tk, tv, tdo;
   if (!make_bshd_map(&tq, q, B, S, H, D) || !make_bshd_map(&tk, k, B, S, Hkv, D) ||

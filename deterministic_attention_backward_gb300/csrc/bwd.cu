@@ -60,13 +60,17 @@ namespace {
 
 // The tile kernel's compile-time mode: bits 0-1 the mask (0 full, 1 causal, 2 causal with an
 // odd tile count under Symmetric Shift), bit 2 the two-strand accumulation of
-// DASH_SCHED_SHIFT_DUAL (D = 128, ordered).  `odd` of the schedule the mode implies:
+// DASH_SCHED_SHIFT_DUAL (ordered).  `odd` of the schedule the mode implies:
 __host__ __device__ constexpr int odd_of(int mode) { return (mode & 3) == 2 ? 1 : 0; }
 __host__ __device__ constexpr bool dual_of(int mode) { return (mode & 4) != 0; }
 
 // Depth of the ring of mbarriers through which the semaphore poller hands a dQ tile's turn
-// to the epilogue (D = 128, ordered variant).
-constexpr int kTurns = 4;
+// to the epilogue (ordered variant): the poller runs at most this many steps ahead
+// (measured: 8 at D = 64, where steps are half as long; 4 at D = 128, 3 % ahead of 8).
+template <int D>
+struct Turns {
+  static constexpr int kN = (D == 64) ? 8 : 4;
+};
 
 template <int D, bool DET>
 struct BwdLayout {
@@ -90,13 +94,13 @@ struct BwdLayout {
   static constexpr int offLSE = offStg + kStgBytes;
   static constexpr int offDVEC = offLSE + kStages * kTile * 4;
   static constexpr int offBar = offDVEC + kStages * kTile * 4;
-  // D = 128, ordered: the poller hands each turn to the epilogue through an mbarrier ring,
-  // on which the epilogue's thread waits suspended instead of spinning on a shared-memory
-  // counter, so it adds no shared-memory loads beside the softmax-gradient warps' traffic
-  // (measured: +3 % at D = 128).  At D = 64 the counter measured faster.
-  static constexpr bool kTurnRing = DET && D == 128;
-  // two-strand mode: a third ring (the epilogue's additions issued, for the releaser warp)
-  // and the ranks of the ring's steps (misc words from offRanks)
+  // Ordered: the poller hands each turn to the epilogue through an mbarrier ring, on which
+  // the epilogue's thread waits suspended instead of spinning on a shared-memory counter
+  // (measured: +3 % at D = 128, equal at D = 64).  Two-strand mode: a third ring (the
+  // epilogue's reductions issued, for the releaser warp) and the ranks of the ring's steps
+  // (misc words from offRanks).
+  static constexpr bool kTurnRing = DET;
+  static constexpr int kTurns = Turns<D>::kN;
   static constexpr int kNumBars = 2 * kStages + 15 + (kTurnRing ? 3 * kTurns : 0);
   static constexpr int offMisc = offBar + kNumBars * 8;
   static constexpr int offRanks = offMisc + 32;
@@ -188,8 +192,8 @@ struct Bars {
     dkv_empty = b + 13;
     drain = b + 14;
     turn_full = L::kTurnRing ? b + 15 : nullptr;  // [kTurns]: the step's semaphore reached its rank
-    turn_empty = L::kTurnRing ? b + 15 + kTurns : nullptr;  // [kTurns]: the step was released
-    added = L::kTurnRing ? b + 15 + 2 * kTurns : nullptr;  // [kTurns]: additions issued (dual)
+    turn_empty = L::kTurnRing ? b + 15 + L::kTurns : nullptr;  // [kTurns]: the step was released
+    added = L::kTurnRing ? b + 15 + 2 * L::kTurns : nullptr;  // [kTurns]: additions issued (dual)
   }
 };
 
@@ -590,19 +594,17 @@ __device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, con
 }
 
 // Semaphore poller (warp 3, deterministic modes): walks this CTA's steps in the
-// epilogue's order and, for each, waits until the step's dQ tile semaphore equals the
-// step's rank, then hands the turn to the epilogue: at D = 128 by arriving on the step's
-// slot of the turn ring (it runs at most kTurns steps ahead), at D = 64 by publishing the
-// number of steps acquired so far in shared memory (any number ahead; safe because a
-// tile's count only grows).  The L2 round trips of the polling thus overlap the
-// computation of the dQ partial instead of following its drain.
+// epilogue's order and, for each, waits until the step's dQ tile semaphore (two strands:
+// the semaphore of the partial's strand) has counted the partials before it, then hands the
+// turn -- and, with two strands, the rank -- to the epilogue by arriving on the step's slot
+// of the turn ring (it runs at most kTurns steps ahead).  The L2 round trips of the polling
+// thus overlap the computation of the dQ partial instead of following its drain.
 template <int D, bool DET, int MODE>
 __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &ab) {
   using L = BwdLayout<D, DET>;
   constexpr bool kDual = dual_of(MODE);
   volatile int *ranks = reinterpret_cast<volatile int *>(smem + L::offRanks);
   const int lane = lane_id();
-  uint32_t *seen = reinterpret_cast<uint32_t *>(smem + L::offMisc + 16);
   const Bars<D, DET> bar(smem);
   uint32_t it = 0;
   const Plan pl = cta_plan(p);
@@ -625,17 +627,12 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
           const int want = kDual ? rank >> 1 : rank;
           int ok = 1;
           if (lane == 0) {
-            if constexpr (L::kTurnRing) {
-              // the slot is free once the epilogue has released the step kTurns earlier
-              const uint32_t slot = it % kTurns, wrap = (it / kTurns) & 1;
-              ok = (mbar_wait(&bar.turn_empty[slot], wrap ^ 1, ab) && sem_wait(sem, want, ab)) ? 1 : 0;
-              if (ok) {
-                if constexpr (kDual) ranks[slot] = rank;
-                mbar_arrive(&bar.turn_full[slot]);
-              }
-            } else {
-              ok = sem_wait(sem, want, ab) ? 1 : 0;
-              if (ok) st_release_cta_shared(seen, it + 1);
+            // the slot is free once the step kTurns earlier has been released
+            const uint32_t slot = it % L::kTurns, wrap = (it / L::kTurns) & 1;
+            ok = (mbar_wait(&bar.turn_empty[slot], wrap ^ 1, ab) && sem_wait(sem, want, ab)) ? 1 : 0;
+            if (ok) {
+              if constexpr (kDual) ranks[slot] = rank;
+              mbar_arrive(&bar.turn_full[slot]);
             }
             // audit record of the executed order (dash_attn_bwd_order_log)
             if (ok && p.order_log) p.order_log[ptile * p.N + kv] = rank;
@@ -674,8 +671,8 @@ __device__ void bwd_releaser(const BwdParams &p, uint8_t *smem, const Bars<D, DE
           const size_t ptile = (size_t)(un.b * p.H + un.hkv * p.G + g) * p.N + q;
           int ok = 1;
           if (lane == 0) {
-            const uint32_t slot = it % kTurns;
-            ok = mbar_wait(&bar.added[slot], (it / kTurns) & 1, ab) ? 1 : 0;
+            const uint32_t slot = it % L::kTurns;
+            ok = mbar_wait(&bar.added[slot], (it / L::kTurns) & 1, ab) ? 1 : 0;
             if (ok) {
               // the slot's rank stays valid until turn_empty lets the poller reuse the slot
               red_release_add(p.sem + ptile * 2 + (ranks[slot] & 1), 1);
@@ -711,7 +708,6 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
   };
   auto agree = [&](bool mine) -> bool { return agree_int(mine ? 1 : 0) != 0; };
   const volatile int *ranks = reinterpret_cast<const volatile int *>(smem + L::offRanks);
-  const uint32_t *seen = reinterpret_cast<const uint32_t *>(smem + L::offMisc + 16);
   constexpr bool kBulk = L::kBulkDQ && !DET;
   const Plan pl = cta_plan(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
@@ -769,15 +765,13 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           // (two strands: thread 0 also reads the partial's rank, and the warpgroup learns
           // its strand with the turn)
           int turn = 1;
-          if constexpr (L::kTurnRing) {
+          if constexpr (DET) {
             if (et == 0)
-              turn = mbar_wait(&bar.turn_full[it % kTurns], (it / kTurns) & 1, ab)
-                         ? (kDual ? 1 + (ranks[it % kTurns] & 1) : 1)
+              turn = mbar_wait(&bar.turn_full[it % L::kTurns], (it / L::kTurns) & 1, ab)
+                         ? (kDual ? 1 + (ranks[it % L::kTurns] & 1) : 1)
                          : 0;
-          } else if constexpr (DET) {
-            if (et == 0) turn = counter_wait(seen, it + 1, ab) ? 1 : 0;
+            turn = agree_int(turn);
           }
-          if (DET) turn = agree_int(turn);
           if (turn == 0) {
             ok = false;
             break;
@@ -801,10 +795,10 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
             named_bar_sync(1, 128);
             if (et == 0) {
               if constexpr (kDual) {
-                mbar_arrive(&bar.added[it % kTurns]);  // the releaser warp releases
+                mbar_arrive(&bar.added[it % L::kTurns]);  // the releaser warp releases
               } else {
                 red_release_add(p.sem + tile_idx, 1);
-                if constexpr (L::kTurnRing) mbar_arrive(&bar.turn_empty[it % kTurns]);
+                mbar_arrive(&bar.turn_empty[it % L::kTurns]);
               }
             }
           }
@@ -890,14 +884,13 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar.dkv_empty, 4);
     mbar_init(bar.drain, 1);
     if constexpr (L::kTurnRing) {
-      for (int i = 0; i < kTurns; ++i) {
+      for (int i = 0; i < L::kTurns; ++i) {
         mbar_init(&bar.turn_full[i], 1);
         mbar_init(&bar.turn_empty[i], 1);
         mbar_init(&bar.added[i], 1);
       }
     }
     *s_abort = 0;
-    *reinterpret_cast<uint32_t *>(smem + L::offMisc + 16) = 0;  // semaphores acquired
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -973,7 +966,7 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 }  // namespace
 
 // MODE bits 0-1: 0 full mask, 1 causal, 2 causal with the padded (odd-N) Symmetric Shift;
-// bit 2: two accumulation strands (ordered, D = 128).  The parity is a constant inside the
+// bit 2: two accumulation strands (ordered).  The parity is a constant inside the
 // kernel, and so is the mask in the full-mask build, which then carries no diagonal or
 // schedule branches of the causal one (measured: +2 %).
 template <int MODE>
@@ -981,7 +974,8 @@ cudaError_t launch_bwd_o(int D, bool deterministic, const CUtensorMap &tq, const
                          const CUtensorMap &tv, const CUtensorMap &tdo, const BwdParams &p, int grid,
                          cudaStream_t stream) {
   if constexpr (dual_of(MODE)) {
-    if (D != 128 || !deterministic) return cudaErrorInvalidValue;
+    if (!deterministic) return cudaErrorInvalidValue;
+    if (D == 64) return launch_bwd_t<64, true, MODE>(tq, tk, tv, tdo, p, grid, stream);
     return launch_bwd_t<128, true, MODE>(tq, tk, tv, tdo, p, grid, stream);
   } else {
     if (D == 64)

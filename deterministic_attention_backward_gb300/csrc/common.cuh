@@ -74,7 +74,7 @@ size_t fwd_smem_bytes(int D);
 
 // mode: bits 0-1: 0 = full mask; 1 = causal mask; 2 = causal mask under Symmetric Shift
 // (shift traversal) with an odd tile count, i.e. the padded schedule; bit 2 (value 4): two
-// accumulation strands (ordered, D = 128 only).  The tile kernel is compiled once per mode.
+// accumulation strands (ordered).  The tile kernel is compiled once per mode.
 // The ordered (deterministic) launch is cooperative: the runtime starts it only with every
 // CTA of the grid resident at once, so a worker never waits on a CTA that cannot start.
 cudaError_t launch_bwd(int D, bool deterministic, int mode, const CUtensorMap &tq,

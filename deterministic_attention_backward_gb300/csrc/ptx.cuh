@@ -448,31 +448,4 @@ __device__ __forceinline__ bool sem_wait(const int *sem, int want, const Abort &
   }
 }
 
-// A counter in shared memory published with release semantics by one warp and awaited
-// with acquire semantics by another (CTA scope).  Bounded like mbar_wait.
-__device__ __forceinline__ void st_release_cta_shared(uint32_t *p, uint32_t v) {
-  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_cta_shared(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-// Spin until the counter reaches at least want (wrap-safe difference).
-__device__ __forceinline__ bool counter_wait(const uint32_t *ctr, uint32_t want, const Abort &ab) {
-  if ((int32_t)(ld_acquire_cta_shared(ctr) - want) >= 0) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if ((int32_t)(ld_acquire_cta_shared(ctr) - want) >= 0) return true;
-    if (ab.set()) return false;
-    if ((it & 63u) == 0) {
-      if (ab.poll_global()) return false;
-      if (globaltimer() - t0 > ab.limit_ns) {
-        ab.raise(kErrSemTimeout);
-        return false;
-      }
-    }
-  }
-}
-
 }  // namespace dash

@@ -93,12 +93,13 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           (dash_sched_resolve names it): the pages leave the choice to the
  *                           user.  Table, from the benchmark's whole-call timings (full mask
  *                           H16 and causal H32 at D = 128 and 64, S = 512 .. 16384, GQA 4:1):
- *                             D = 64, or N < 8                    -> SHIFT_FILL
- *                             D = 128, full mask                  -> SHIFT_DUAL (+5 % at
- *                                                                    N = 8, +16 % at N = 128)
+ *                             N < 8                               -> SHIFT_FILL
+ *                             full mask                           -> SHIFT_DUAL (D = 128:
+ *                                                                    +5 % at N = 8, +16 % at
+ *                                                                    N = 128; D = 64: +12 %)
  *                             D = 128, causal, G > 1              -> SHIFT_DUAL (+8 %, N = 64)
  *                             D = 128, causal, G = 1, N >= 64     -> SHIFT_DUAL (+0.5-3 %)
- *                             D = 128, causal, G = 1, N < 64      -> SHIFT_FILL (2-8 % ahead)
+ *                             otherwise (causal)                  -> SHIFT_FILL (2-10 % ahead)
  *  DASH_SCHED_SHIFT_DUAL -- packed Shift Scheduling (the SHIFT_FILL traversal, grid and ranks)
  *                           with each dQ tile accumulated in two strands: the partial of rank
  *                           r is added into strand r mod 2 as that strand's (r div 2)-th
@@ -108,7 +109,6 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *                           single chain of the pages: a strand's next contributor comes two
  *                           lock steps later instead of one, which lets the kernel spread its
  *                           reductions out and release each strand from a separate warp.
- *                           D = 128 only (DASH_ERR_UNSUPPORTED at D = 64).
  */
 typedef enum {
   DASH_SCHED_ATOMIC = 0,

@@ -71,8 +71,6 @@ def test_full_size_sampled_rows_match_oracle(dash, cfg):
     qr, kr = sample_rows(S, 1), sample_rows(S, 2)
     refs = {bg: oracle.attn_bwd_rows(*host, causal, bg[0], bg[1], qr, kr) for bg in groups}
     for s in SCHEDULES:
-        if s == "shift_dual" and D != 128:
-            continue
         grads = dash.bwd(q, k, v, o, do, lse, causal=causal, schedule=s, workspace=ws)
         dash.status(ws)
         for b, g in groups:
@@ -86,20 +84,24 @@ def test_full_size_sampled_rows_match_oracle(dash, cfg):
 @pytest.mark.parametrize("causal,S", [(False, 160 * 128), (True, 320 * 128), (True, 319 * 128)])
 def test_heads_wider_than_the_grid(dash, causal, S):
     """More shift workers per head than SMs (full: N = 160; causal: 160 pairs, also for
-    the odd N = 319): the packed schedule (and AUTO) runs the head in several rounds;
-    sampled rows match the oracle and repeats are bit-identical."""
+    the odd N = 319): the packed schedules (single and two strands, and AUTO) run the head in
+    several rounds; sampled rows match the oracle, and AUTO gives the bits of the schedule
+    it resolves to."""
     B, H, Hkv, D = 1, 2, 1, 64
     host = make_qkv_do(B, S, H, Hkv, D, seed=4)
     q, k, v, do = (t.cuda() for t in host)
     o, lse = dash.fwd(q, k, v, causal=causal, check=True)
-    first = [t.clone() for t in dash.bwd(q, k, v, o, do, lse, causal=causal,
-                                         schedule="shift_fill", check=True)]
+    resolved = dash.sched_resolve("auto", causal, S // 128, D, H // Hkv)
+    runs = {s: [t.clone() for t in dash.bwd(q, k, v, o, do, lse, causal=causal, schedule=s,
+                                            check=True)]
+            for s in ("shift_fill", "shift_dual")}
     again = dash.bwd(q, k, v, o, do, lse, causal=causal, schedule="auto", check=True)
-    for a, b in zip(first, again):
+    for a, b in zip(runs[resolved], again):
         assert torch.equal(a, b)
     qr, kr = sample_rows(S, 5), sample_rows(S, 6)
     sq, sk, sv = oracle.attn_bwd_rows(*host, causal, 0, 0, qr, kr)
-    dq, dk, dv = (t.detach().to(torch.float64).cpu().numpy() for t in first)
-    close("dQ", dq[0, qr], sq)
-    close("dK", dk[0, kr, 0], sk)
-    close("dV", dv[0, kr, 0], sv)
+    for s, grads in runs.items():
+        dq, dk, dv = (t.detach().to(torch.float64).cpu().numpy() for t in grads)
+        close(f"{s} dQ", dq[0, qr], sq)
+        close(f"{s} dK", dk[0, kr, 0], sk)
+        close(f"{s} dV", dv[0, kr, 0], sv)

@@ -68,11 +68,6 @@ def test_fwd_matches_oracle(dash, shape, causal):
 @pytest.mark.parametrize("shape", SHAPES)
 def test_bwd_matches_oracle(dash, shape, causal, sched):
     c = Case(dash, *shape, causal)
-    if sched == "shift_dual" and shape[4] == 64:  # the two-strand kernel is D = 128 only
-        with pytest.raises(dash.DashError) as err:
-            c.bwd(sched)
-        assert err.value.code == 2
-        return
     dq_r, dk_r, dv_r, _, _ = oracle.attn_bwd(*c.host, causal)
     dq, dk, dv = c.bwd(sched)
     close("dQ", dq, dq_r)
@@ -107,8 +102,6 @@ def test_causal_first_query_row_dq_vanishes(dash):
     is zero up to the rounding of P, O and the two dot products."""
     c = Case(dash, 1, 512, 2, 2, 64, True, seed=3)
     for sched in SCHEDULES:
-        if sched == "shift_dual":  # D = 64 here
-            continue
         dq, _, _ = c.bwd(sched)
         assert dq[:, 0].abs().max().item() <= 1e-2 * dq.abs().max().item(), sched
 

@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 REL_FRO = 1e-2
 MAX_ABS = 2e-2
-SCHEDULES = ["atomic", "serial", "descending", "shift", "shift_fill", "auto"]
+SCHEDULES = ["atomic", "serial", "descending", "shift", "shift_fill", "shift_dual", "auto"]
 RAGGED = [  # (B, S, H, Hkv, D)
     (1, 200, 2, 2, 64),     # 2 tiles, the second 72 rows
     (2, 333, 2, 1, 128),    # 3 tiles, GQA 2:1, two batches (rows past S must not spill into
