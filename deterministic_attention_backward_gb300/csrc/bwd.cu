@@ -629,7 +629,10 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
           if (lane == 0) {
             // the slot is free once the step kTurns earlier has been released
             const uint32_t slot = it % L::kTurns, wrap = (it / L::kTurns) & 1;
-            ok = (mbar_wait(&bar.turn_empty[slot], wrap ^ 1, ab) && sem_wait(sem, want, ab)) ? 1 : 0;
+            ok = mbar_wait(&bar.turn_empty[slot], wrap ^ 1, ab) ? 1 : 0;
+            DASH_TRACE(p, 29);
+            ok = ok && sem_wait(sem, want, ab) ? 1 : 0;
+            DASH_TRACE(p, 30);
             if (ok) {
               if constexpr (kDual) ranks[slot] = rank;
               mbar_arrive(&bar.turn_full[slot]);
@@ -645,8 +648,8 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
 }
 
 // Releaser (warp 2 in the two-strand mode, after it has allocated the tensor memory): once
-// the epilogue warpgroup has issued a step's reductions (its threads met at a named barrier,
-// then one of them arrived on the step's `added` slot), advances the semaphore of the step's
+// the epilogue warpgroup has issued a step's reductions (each of its four warps arrived on
+// the step's `added` slot after its own), advances the semaphore of the step's
 // dQ tile and strand by one with gpu-scope release semantics -- which orders every one of
 // those reductions before it -- and frees the turn-ring slot for the poller.  The release
 // waits until the reductions are performed; done here, that wait does not hold the
@@ -676,6 +679,7 @@ __device__ void bwd_releaser(const BwdParams &p, uint8_t *smem, const Bars<D, DE
             if (ok) {
               // the slot's rank stays valid until turn_empty lets the poller reuse the slot
               red_release_add(p.sem + ptile * 2 + (ranks[slot] & 1), 1);
+              DASH_TRACE(p, 31);
               mbar_arrive(&bar.turn_empty[slot]);
             }
           }
@@ -721,7 +725,20 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           const int h = un.hkv * p.G + g;
           const int q = step_q(pl.sched, mode_causal<MODE>(p), p.N, un.w, seg, t, odd_of(MODE));
           const size_t tile_idx = (size_t)(un.b * p.H + h) * p.N + q;
-          if (!agree(et == 0 ? mbar_wait(bar.g5_done, it & 1, ab) : true)) {
+          // two strands: thread 0 also takes the step's turn before the warpgroup meets, and
+          // the strand travels with the decision, so no second barrier follows the drain (the
+          // turn is normally ready thousands of cycles before the dQ partial; measured: the
+          // separate wait and barrier after the drain cost ~540 cycles a step)
+          int g5 = 1;
+          if (et == 0) {
+            g5 = mbar_wait(bar.g5_done, it & 1, ab) ? 1 : 0;
+            if (kDual && g5)
+              g5 = mbar_wait(&bar.turn_full[it % L::kTurns], (it / L::kTurns) & 1, ab)
+                       ? 1 + (ranks[it % L::kTurns] & 1)
+                       : 0;
+          }
+          g5 = agree_int(g5);
+          if (!g5) {
             ok = false;
             break;
           }
@@ -761,15 +778,15 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
             continue;
           }
           // the semaphore counts the partials added so far: the contributor of rank r goes
-          // once rank r-1 has released it; the poller warp has been watching it
-          // (two strands: thread 0 also reads the partial's rank, and the warpgroup learns
-          // its strand with the turn)
-          int turn = 1;
-          if constexpr (DET) {
-            if (et == 0)
-              turn = mbar_wait(&bar.turn_full[it % L::kTurns], (it / L::kTurns) & 1, ab)
-                         ? (kDual ? 1 + (ranks[it % L::kTurns] & 1) : 1)
-                         : 0;
+          // once rank r-1 has released it; the poller warp has been watching it (single
+          // strand: the turn is taken here; two strands: with the G5 wait above, as 1 + the
+          // strand of the partial)
+          int turn = g5;
+          if constexpr (DET && !kDual) {
+            if (et == 0) {
+              turn = mbar_wait(&bar.turn_full[it % L::kTurns], (it / L::kTurns) & 1, ab) ? 1 : 0;
+              DASH_TRACE(p, 28);
+            }
             turn = agree_int(turn);
           }
           if (turn == 0) {
@@ -791,15 +808,14 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
                 __nanosleep(kRedPaceNs);
             }
           }
-          if (DET) {  // one release for the warpgroup, after all of its reductions
+          if constexpr (kDual) {  // each warp's reductions issued: the releaser releases
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.added[it % L::kTurns]);
+          } else if constexpr (DET) {  // one release for the warpgroup, after all reductions
             named_bar_sync(1, 128);
             if (et == 0) {
-              if constexpr (kDual) {
-                mbar_arrive(&bar.added[it % L::kTurns]);  // the releaser warp releases
-              } else {
-                red_release_add(p.sem + tile_idx, 1);
-                mbar_arrive(&bar.turn_empty[it % L::kTurns]);
-              }
+              red_release_add(p.sem + tile_idx, 1);
+              mbar_arrive(&bar.turn_empty[it % L::kTurns]);
             }
           }
           if (et == 0) DASH_TRACE(p, 17);
@@ -887,7 +903,7 @@ __global__ void __launch_bounds__(512, 1)
       for (int i = 0; i < L::kTurns; ++i) {
         mbar_init(&bar.turn_full[i], 1);
         mbar_init(&bar.turn_empty[i], 1);
-        mbar_init(&bar.added[i], 1);
+        mbar_init(&bar.added[i], 4);  // the four epilogue warps (two-strand mode)
       }
     }
     *s_abort = 0;
