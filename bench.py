@@ -68,7 +68,7 @@ def schedules_for(D):
     return list(SCHEDULES)
 FALLBACK_PEAK_TFLOPS = 1900.0   # only if the measured-peaks file is absent
 PROFILE = os.path.join(ROOT, "profiles", "bwd_tile_kernel_full_h16_d128.md")
-KERNEL_SOURCES = ["bwd.cu", "ptx.cuh", "sched.cuh", "common.cuh"]
+KERNEL_SOURCES = ["bwd_kernel.cuh", "ptx.cuh", "sched.cuh", "common.cuh"]
 
 
 def bwd_flops(B, S, H, D, causal):
@@ -349,6 +349,7 @@ def run_gpu(args, wl, rank, world):
 
     configs = None if (args.no_configs or args.quick) else other_configs(args, dev, dash)
     block = None if (args.no_block or args.quick) else block_timing()
+    varlen = None if (args.no_varlen or args.quick) else varlen_timing(dev, dash)
 
     peak, peak_sus, peak_kind = peaks()
     value = job_tflops(step_flops, args.steps, world, elapsed_ms)
@@ -389,6 +390,8 @@ def run_gpu(args, wl, rank, world):
         res["configs"] = configs
     if block is not None:
         res["block"] = block
+    if varlen is not None:
+        res["varlen"] = varlen
     return res
 
 
@@ -448,6 +451,81 @@ def other_configs(args, dev, dash):
             del q, k, v, do, o, lse, ws, dq, dk, dv
             torch.cuda.empty_cache()
         out[name] = {"description": wl["desc"], "points": rows}
+    return out
+
+
+VARLEN = {"n": 64, "lo": 64, "hi": 4096, "H": 32, "Hkv": 8, "D": 128, "causal": True, "seed": 0}
+
+
+def varlen_lengths(cfg=VARLEN):
+    """Seeded sequence lengths of the packed batch: log-uniform in [lo, hi]."""
+    import numpy as np
+    rng = np.random.default_rng(cfg["seed"])
+    x = rng.uniform(np.log(cfg["lo"]), np.log(cfg["hi"]), size=cfg["n"])
+    return [int(round(float(np.exp(t)))) for t in x]
+
+
+def varlen_timing(dev, dash, cfg=VARLEN):
+    """A packed causal batch of 64 sequences (log-uniform 64..4096 tokens, GQA 32/8 heads,
+    D = 128): the whole varlen backward call with every sequence's heads in one tile-kernel
+    launch (packed schedules and atomic) against one B = 1 call per sequence (the same
+    schedule, AUTO), median of 3 after a warm-up."""
+    import numpy as np
+    import torch
+    lengths = varlen_lengths(cfg)
+    H, Hkv, D, causal = cfg["H"], cfg["Hkv"], cfg["D"], cfg["causal"]
+    T = sum(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    g = torch.Generator(device=dev).manual_seed(0)
+    q = torch.randn(T, H, D, device=dev, generator=g).to(torch.bfloat16)
+    k = torch.randn(T, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
+    do = torch.randn(T, H, D, device=dev, generator=g).to(torch.bfloat16)
+    o, lse = dash.fwd_varlen(q, k, v, cu, causal=causal, check=True)
+    ws = torch.empty(dash.bwd_varlen_workspace_bytes(cu, H, D), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flops = sum(bwd_flops(1, S, H, D, causal) for S in lengths)
+    slices = []
+    for b, S in enumerate(lengths):
+        s0 = int(cu[b])
+        sl = lambda t: t[s0:s0 + S].unsqueeze(0)
+        slices.append((sl(q), sl(k), sl(v), sl(o), sl(do),
+                       lse[s0 * H:(s0 + S) * H].view(1, H, S), sl(dq), sl(dk), sl(dv)))
+
+    def packed(s):
+        dash.bwd_varlen(q, k, v, o, do, lse, cu, causal=causal, schedule=s, dq=dq, dk=dk, dv=dv,
+                        workspace=ws)
+
+    def loop(s):
+        for (q1, k1, v1, o1, do1, l1, dq1, dk1, dv1) in slices:
+            dash.bwd(q1, k1, v1, o1, do1, l1, causal=causal, schedule=s, dq=dq1, dk=dk1,
+                     dv=dv1, workspace=ws)
+    runs = {"packed_" + s: (lambda s=s: packed(s)) for s in ("atomic", "shift_fill", "shift_dual", "auto")}
+    runs["per_sequence_auto"] = lambda: loop("auto")
+    runs["per_sequence_atomic"] = lambda: loop("atomic")
+    for f in runs.values():
+        f()
+    dash.status(ws)
+    ev = {n: [] for n in runs}
+    for _ in range(3):
+        for n, f in runs.items():
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            f()
+            b.record()
+            ev[n].append((a, b))
+    torch.cuda.synchronize()
+    dash.status(ws)
+    out = {"description": "packed causal batch, " + str(cfg["n"]) + " sequences of "
+                          f"{min(lengths)}..{max(lengths)} tokens (log-uniform, seeded), "
+                          f"{T} tokens, H={H} Hkv={Hkv} D={D}; TFLOP/s of the whole backward call",
+           "tokens": T}
+    for n in runs:
+        out[n + "_tflops"] = round(flops / statistics.median(a.elapsed_time(b) for a, b in ev[n]) / 1e9, 1)
+    auto = dash.sched_resolve("auto", causal, (max(lengths) + 127) // 128, D, H // Hkv)
+    out["auto_runs"] = auto
+    out["packed_speedup_vs_per_sequence"] = round(out["packed_auto_tflops"] / out["per_sequence_auto_tflops"], 3)
+    out["packed_auto_slowdown_vs_atomic"] = round(out["packed_atomic_tflops"] / out["packed_auto_tflops"] - 1, 4)
     return out
 
 
@@ -539,6 +617,8 @@ def main():
                     help="skip the per-schedule table of the other workloads")
     ap.add_argument("--no-block", action="store_true",
                     help="skip the transformer-block timing")
+    ap.add_argument("--no-varlen", action="store_true",
+                    help="skip the packed variable-length batch timing")
     ap.add_argument("--seq", type=int, default=0,
                     help="run one sequence length of the workload's sweep only")
     ap.add_argument("--quick", action="store_true",

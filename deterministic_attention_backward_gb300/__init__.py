@@ -21,7 +21,8 @@ import threading
 __all__ = ["fwd", "bwd", "bwd_workspace_bytes", "fwd_workspace_bytes", "status",
            "bwd_order_log", "set_wait_limit", "wait_limit", "sched_table", "sched_grid",
            "sched_workers",
-           "sched_resolve", "packed_rank", "fwd_varlen", "bwd_varlen", "SCHEDULES", "lib",
+           "sched_resolve", "packed_rank", "fwd_varlen", "bwd_varlen", "bwd_varlen_workspace_bytes",
+           "bwd_varlen_order_log", "SCHEDULES", "lib",
            "DashError"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +42,7 @@ EXPORTS = ["dash_attn_fwd_workspace_bytes", "dash_attn_fwd", "dash_attn_bwd_work
            "dash_status_string", "dash_sched_workers", "dash_sched_segments", "dash_sched_steps",
            "dash_sched_step", "dash_sched_grid", "dash_sched_packed_rank", "dash_sched_resolve",
            "dash_attn_bwd_noalloc", "dash_attn_bwd_varlen_workspace_bytes",
-           "dash_attn_fwd_varlen", "dash_attn_bwd_varlen"]
+           "dash_attn_fwd_varlen", "dash_attn_bwd_varlen", "dash_attn_bwd_varlen_order_log"]
 
 
 class DashError(RuntimeError):
@@ -88,6 +89,9 @@ def lib() -> ctypes.CDLL:
         L.dash_attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, i, i, i, i, f,
                                            i, i, vp, sz, vp]
         L.dash_attn_bwd_varlen.restype = i
+        L.dash_attn_bwd_varlen_order_log.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, i, i,
+                                                     i, i, f, i, i, vp, sz, vp, vp]
+        L.dash_attn_bwd_varlen_order_log.restype = i
         L.dash_attn_status.argtypes = [vp, vp]
         L.dash_attn_status.restype = i
         L.dash_attn_bwd_status.argtypes = [vp, vp]
@@ -356,12 +360,18 @@ def fwd_varlen(q, k, v, cu_seqlens, causal: bool = False, scale: float | None = 
     return o, lse
 
 
-def bwd_varlen(q, k, v, o, do, lse, cu_seqlens, causal: bool = False, schedule: str = "auto",
-               scale: float | None = None, stream=None, check: bool = False):
-    """Backward over a packed batch (layouts as ``fwd_varlen``): returns dQ, dK, dV."""
+def bwd_varlen_workspace_bytes(cu_seqlens, H: int, D: int) -> int:
+    """Workspace bytes of ``bwd_varlen`` for these sequence offsets (0 if unsupported)."""
+    _, batch, cp = _cu(cu_seqlens)
+    return int(lib().dash_attn_bwd_varlen_workspace_bytes(cp, batch, H, D))
+
+
+def _bwd_varlen_call(q, k, v, o, do, lse, cu_seqlens, causal, schedule, scale, stream, dq, dk,
+                     dv, workspace, order):
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
         _require(t, n, torch.bfloat16)
+    _require(lse, "lse", torch.float32)
     T, H, D = q.shape
     Hkv = k.shape[1]
     cu, batch, cp = _cu(cu_seqlens)
@@ -369,16 +379,52 @@ def bwd_varlen(q, k, v, o, do, lse, cu_seqlens, causal: bool = False, schedule: 
         raise ValueError("cu_seqlens[-1] must equal the number of tokens")
     if schedule not in SCHEDULES:
         raise ValueError(f"schedule must be one of {sorted(SCHEDULES)}")
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    nbytes = lib().dash_attn_bwd_varlen_workspace_bytes(cp, batch, H, D)
-    ws = _workspace(max(int(nbytes), 256), q.device)
-    code = lib().dash_attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                      do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                      dv.data_ptr(), cp, batch, H, H // Hkv, D,
-                                      float(scale) if scale else 0.0, int(bool(causal)),
-                                      SCHEDULES[schedule], ws.data_ptr(), ws.numel(),
-                                      _stream_ptr(stream))
-    _check(code, "dash_attn_bwd_varlen")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        nbytes = lib().dash_attn_bwd_varlen_workspace_bytes(cp, batch, H, D)
+        workspace = _workspace(max(int(nbytes), 256), q.device)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cp, batch, H, H // Hkv,
+            D, float(scale) if scale else 0.0, int(bool(causal)), SCHEDULES[schedule],
+            workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    if order is None:
+        code = lib().dash_attn_bwd_varlen(*args, _stream_ptr(stream))
+        _check(code, "dash_attn_bwd_varlen")
+    else:
+        code = lib().dash_attn_bwd_varlen_order_log(*args, order.data_ptr(), _stream_ptr(stream))
+        _check(code, "dash_attn_bwd_varlen_order_log")
+    return dq, dk, dv, workspace
+
+
+def bwd_varlen(q, k, v, o, do, lse, cu_seqlens, causal: bool = False, schedule: str = "auto",
+               scale: float | None = None, stream=None, check: bool = False, dq=None, dk=None,
+               dv=None, workspace=None):
+    """Backward over a packed batch (layouts as ``fwd_varlen``): returns dQ, dK, dV.  The
+    packed schedules (``shift_fill``, ``shift_dual``, ``auto``) and ``atomic`` run every
+    sequence in one tile-kernel launch; the others one sequence after another."""
+    dq, dk, dv, ws = _bwd_varlen_call(q, k, v, o, do, lse, cu_seqlens, causal, schedule, scale,
+                                      stream, dq, dk, dv, workspace, None)
     if check:
         status(ws, stream)
     return dq, dk, dv
+
+
+def bwd_varlen_order_log(q, k, v, o, do, lse, cu_seqlens, causal: bool = False,
+                         schedule: str = "shift_fill", scale: float | None = None, stream=None):
+    """``bwd_varlen`` through ``dash_attn_bwd_varlen_order_log``: returns (dQ, dK, dV,
+    order) with order [tiles, Nmax] int32 (the non-empty sequences' [H, N_b] tiles one after
+    another; -1 where no partial was added)."""
+    import torch
+    import numpy as np
+    cu, _, _ = _cu(cu_seqlens)
+    H = q.shape[1]
+    lens = np.diff(cu)
+    ns = (lens + 127) // 128
+    order = torch.full((int(H * ns.sum()), max(int(ns.max()), 1)), -1, dtype=torch.int32,
+                       device=q.device)
+    dq, dk, dv, ws = _bwd_varlen_call(q, k, v, o, do, lse, cu_seqlens, causal, schedule, scale,
+                                      stream, None, None, None, None, order)
+    status(ws, stream)
+    return dq, dk, dv, order

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdash_attn.so")
-SOURCES = ["api.cu", "bwd.cu", "fwd.cu", "aux.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "bwd.cu", "bwd_varlen.cu", "fwd.cu", "aux.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

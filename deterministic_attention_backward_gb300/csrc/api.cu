@@ -47,6 +47,21 @@ bool make_bshd_map(CUtensorMap *m, const void *base, int B, int S, int Hx, int D
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [T, Hx, D] bf16 packed tokens viewed as a 3-D tensor (D, Hx, T), same box and swizzle as
+// make_bshd_map.  Rows past T read as zeros; a sequence's rows past its end are the next
+// sequence's tokens, which the tile kernel masks.
+bool make_thd_map(CUtensorMap *m, const void *base, int T, int Hx, int D) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hx, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hx * D * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)dash::kBoxCols, 1, (cuuint32_t)kTile};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ device properties
 struct DevInfo {
   int sms = 0, major = 0, minor = 0;
@@ -101,10 +116,10 @@ struct BwdWorkspace {
 // [status 256 B][semaphores][lse2][Dvec][dQ accumulator], each part 256-byte aligned; the
 // status block and the semaphores are contiguous so that one clear covers both.  Row arrays
 // are per tile: S padded up to N*128 rows per (b, h).  Semaphores and accumulator have room
-// for kMaxStrands strands per dQ tile (a call with K strands uses [B,H,N][K]...).
-BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
+// for kMaxStrands strands per dQ tile (a call with K strands uses [B,H,N][K]...).  `ntiles`
+// dQ tiles in all (B*H*N for a uniform batch).
+BwdWorkspace carve_tiles(void *ws, size_t ntiles, int D) {
   BwdWorkspace w{};
-  const size_t ntiles = (size_t)B * H * tiles(S);
   const size_t rows = ntiles * kTile;
   char *base = static_cast<char *>(ws);
   size_t off = 0;
@@ -122,6 +137,9 @@ BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
   off = align256(off + w.dqacc_bytes * dash::kMaxStrands);
   w.total = off;
   return w;
+}
+BwdWorkspace carve_bwd(void *ws, int B, int S, int H, int D) {
+  return carve_tiles(ws, (size_t)B * H * tiles(S), D);
 }
 
 // Limit of one bounded wait inside the kernels (dash_attn_set_wait_limit).
@@ -238,7 +256,7 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
                               int B, int S, int H, int group, int D, float scale,
                               dash_mask_t mask, dash_sched_t sched, void *workspace,
                               size_t workspace_bytes, unsigned stages, dash_stream_t stream,
-                              bool keep_status, int *order_log) {
+                              bool keep_status, int *order_log, int log_stride = 0) {
   if (stages == 0 || (stages & ~unsigned(DASH_BWD_ALL))) return DASH_ERR_INVALID;
   dash_status_t st = check_sizes(B, S, H, group, D);
   if (st != DASH_OK) return st;
@@ -298,6 +316,7 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   p.dk = static_cast<__nv_bfloat16 *>(dk);
   p.dv = static_cast<__nv_bfloat16 *>(dv);
   p.order_log = ordered ? order_log : nullptr;
+  p.log_stride = log_stride > 0 ? log_stride : N;
   p.B = B;
   p.S = S;
   p.H = H;
@@ -372,8 +391,13 @@ dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const v
 }
 
 // ------------------------------------------------------------------ variable-length batches
-// The sequences of a packed batch are independent attention problems: each runs as the
-// B = 1 problem on its own slices, one after another on `stream`, sharing the workspace.
+// The sequences of a packed batch are independent attention problems.  With the packed
+// schedules (SHIFT_FILL, SHIFT_DUAL, AUTO, which resolves to one of them) and ATOMIC, the
+// workers of every sequence's heads are dealt onto the persistent grid together, one launch
+// per group of at most dash::kMaxVarlenSeqs non-empty sequences; each sequence keeps its own
+// tile count and accumulation order (the packed shift ranks at the sequence's position in
+// the launch).  The single-round schedules (SERIAL, DESCENDING, SHIFT) run each sequence as
+// the B = 1 problem on its own slices, one after another on `stream`.
 static dash_status_t check_seqlens(const int *cu, int batch, int *max_len) {
   if (!cu || batch <= 0 || cu[0] != 0) return DASH_ERR_INVALID;
   int mx = 0;
@@ -385,10 +409,71 @@ static dash_status_t check_seqlens(const int *cu, int batch, int *max_len) {
   return DASH_OK;
 }
 
+// One launch of the packed varlen path: sequences [b0, b1) of the batch (b1 - b0 non-empty
+// ones at most dash::kMaxVarlenSeqs), their tokens [tok0, tok1), tiles and workers.
+struct VarlenGroup {
+  int b0, b1, tok0, tok1, nseq, units;
+  size_t ntiles;
+  bool ragged;
+};
+
+// The next group from sequence b on (empty sequences are skipped).
+VarlenGroup next_group(const int *cu, int batch, int b, int H, int Hkv, int causal) {
+  VarlenGroup g{};
+  g.b0 = b;
+  g.tok0 = cu[b];
+  long long units = 0;
+  while (b < batch && g.nseq < dash::kMaxVarlenSeqs) {
+    const int S = cu[b + 1] - cu[b];
+    ++b;
+    if (S == 0) continue;
+    const int N = tiles(S);
+    g.ntiles += (size_t)H * N;
+    units += (long long)Hkv * dash::sched_workers(dash::kShift, causal, N, causal ? (N & 1) : 0);
+    g.ragged |= (S % kTile) != 0;
+    ++g.nseq;
+  }
+  g.b1 = b;
+  g.tok1 = cu[b];
+  g.units = units > (1LL << 30) ? -1 : (int)units;
+  return g;
+}
+
+size_t table_bytes() {
+  return align256(sizeof(int4) * dash::kMaxVarlenSeqs) + align256(sizeof(int) * (dash::kMaxVarlenSeqs + 1));
+}
+
+size_t packed_bytes(const VarlenGroup &g, int D) {
+  return carve_tiles(nullptr, g.ntiles, D).total + table_bytes();
+}
+
+bool packed_sched(int sched) {
+  return sched == DASH_SCHED_ATOMIC || sched == DASH_SCHED_SHIFT_FILL ||
+         sched == DASH_SCHED_SHIFT_DUAL;
+}
+
+// Workspace of the packed path: the largest group's; validates sizes (0 = invalid).
+size_t varlen_packed_bytes(const int *cu, int batch, int H, int group, int D, int causal) {
+  size_t need = 0;
+  for (int b = 0; b < batch;) {
+    const VarlenGroup g = next_group(cu, batch, b, H, H / group, causal);
+    if (g.units < 0 || g.ntiles >= (size_t)1 << 30 || g.tok1 - g.tok0 >= (1 << 30)) return 0;
+    const size_t n = packed_bytes(g, D);
+    need = n > need ? n : need;
+    b = g.b1;
+  }
+  return need;
+}
+
 size_t dash_attn_bwd_varlen_workspace_bytes(const int *cu_seqlens, int batch, int H, int D) {
   int mx = 0;
   if (check_seqlens(cu_seqlens, batch, &mx) != DASH_OK || mx == 0) return 0;
-  return dash_attn_bwd_workspace_bytes(1, mx, H, D);
+  const size_t single = dash_attn_bwd_workspace_bytes(1, mx, H, D);
+  if (single == 0) return 0;
+  // either mask (the causal workers differ, the tiles do not); group 1 (tiles do not depend on it)
+  const size_t packed = varlen_packed_bytes(cu_seqlens, batch, H, 1, D, 1);
+  if (packed == 0) return 0;
+  return packed > single ? packed : single;
 }
 
 dash_status_t dash_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
@@ -416,33 +501,154 @@ dash_status_t dash_attn_fwd_varlen(const void *q, const void *k, const void *v, 
   return DASH_OK;
 }
 
-dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
-                                   const void *dout, const float *lse, void *dq, void *dk,
-                                   void *dv, const int *cu_seqlens, int batch, int H, int group,
-                                   int D, float scale, dash_mask_t mask, dash_sched_t sched,
-                                   void *workspace, size_t workspace_bytes,
-                                   dash_stream_t stream) {
+// One packed launch sequence (clears, sequence table, preprocess, tile kernel, dQ convert)
+// for group g; pointers are the batch's, offset here to the group's first token.
+static dash_status_t bwd_varlen_group(const VarlenGroup &g, const int *cu, const void *q,
+                                      const void *k, const void *v, const void *o,
+                                      const void *dout, const float *lse, void *dq, void *dk,
+                                      void *dv, int H, int group, int D, float sc, int causal,
+                                      int sched, int sms, void *workspace, cudaStream_t s,
+                                      bool keep_status, int *order_log, int log_stride) {
+  using bf = __nv_bfloat16;
+  const int Hkv = H / group, T = g.tok1 - g.tok0;
+  const size_t qo = (size_t)g.tok0 * H * D, ko = (size_t)g.tok0 * Hkv * D;
+  const bool ordered = sched != DASH_SCHED_ATOMIC;
+  const int K = sched == DASH_SCHED_SHIFT_DUAL ? 2 : 1;
+  const BwdWorkspace w = carve_tiles(workspace, g.ntiles, D);
+  int4 *seqs = reinterpret_cast<int4 *>(static_cast<char *>(workspace) + w.total);
+  int *wprefix = reinterpret_cast<int *>(reinterpret_cast<char *>(seqs) +
+                                         align256(sizeof(int4) * dash::kMaxVarlenSeqs));
+  // the sequence table, tokens relative to the group's first
+  static thread_local dash::VarlenTable t;
+  int n = 0, tile = 0, unit = 0;
+  for (int b = g.b0; b < g.b1; ++b) {
+    const int S = cu[b + 1] - cu[b];
+    if (S == 0) continue;
+    const int N = tiles(S);
+    t.seqs[n] = make_int4(S, cu[b] - g.tok0, tile, N);
+    t.wprefix[n] = unit;
+    tile += H * N;
+    unit += Hkv * dash::sched_workers(dash::kShift, causal, N, causal ? (N & 1) : 0);
+    ++n;
+  }
+  t.wprefix[n] = unit;
+  t.batch = n;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_thd_map(&tq, static_cast<const bf *>(q) + qo, T, H, D) ||
+      !make_thd_map(&tk, static_cast<const bf *>(k) + ko, T, Hkv, D) ||
+      !make_thd_map(&tv, static_cast<const bf *>(v) + ko, T, Hkv, D) ||
+      !make_thd_map(&tdo, static_cast<const bf *>(dout) + qo, T, H, D))
+    return DASH_ERR_CUDA;
+  if ((keep_status ? cudaMemsetAsync(w.sem, 0, w.sem_bytes, s)
+                   : cudaMemsetAsync(w.status, 0, kStatusBytes + w.sem_bytes, s)) != cudaSuccess ||
+      cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes * K, s) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  if (g.ragged &&
+      cudaMemsetAsync(w.lse2, 0, reinterpret_cast<char *>(w.dqacc) - reinterpret_cast<char *>(w.lse2),
+                      s) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  if (dash::launch_varlen_setup(t, seqs, wprefix, s) != cudaSuccess ||
+      dash::launch_preprocess_varlen(static_cast<const bf *>(o) + qo,
+                                     static_cast<const bf *>(dout) + qo, lse + (size_t)g.tok0 * H,
+                                     w.dvec, w.lse2, seqs, n, T, H, D, s) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  dash::BwdParams p{};
+  p.lse2 = w.lse2;
+  p.dvec = w.dvec;
+  p.dqacc = w.dqacc;
+  p.sem = w.sem;
+  p.status = w.status;
+  p.dk = static_cast<bf *>(dk) + ko;
+  p.dv = static_cast<bf *>(dv) + ko;
+  p.order_log = ordered ? order_log : nullptr;
+  p.log_stride = log_stride;
+  p.seqs = seqs;
+  p.seq_wprefix = wprefix;
+  p.batch = n;
+  p.units = unit;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = group;
+  p.causal = causal;
+  p.sched = dash::kShift;
+  p.packed = sched == DASH_SCHED_SHIFT_FILL || sched == DASH_SCHED_SHIFT_DUAL;
+  p.wait_ns = g_wait_ns.load();
+  p.scale_log2 = sc * dash::kLog2e;
+  p.scale = sc;
+#ifdef DASH_TRACE_BUILD
+  p.trace = g_trace;
+  p.trace_cta = g_trace_cta;
+#endif
+  const int grid = unit < sms ? unit : sms;
+  if (dash::launch_bwd_varlen(D, ordered, causal, K > 1, tq, tk, tv, tdo, p, grid, s) !=
+          cudaSuccess ||
+      dash::launch_dq_convert_varlen(w.dqacc, static_cast<bf *>(dq) + qo, sc, seqs, n, T, H, D,
+                                     K, s) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  return DASH_OK;
+}
+
+static dash_status_t bwd_varlen_impl(const void *q, const void *k, const void *v, const void *o,
+                                     const void *dout, const float *lse, void *dq, void *dk,
+                                     void *dv, const int *cu_seqlens, int batch, int H,
+                                     int group, int D, float scale, dash_mask_t mask,
+                                     dash_sched_t sched, void *workspace, size_t workspace_bytes,
+                                     dash_stream_t stream, int *order_log) {
   int mx = 0;
   dash_status_t st = check_seqlens(cu_seqlens, batch, &mx);
   if (st != DASH_OK) return st;
   if (H <= 0 || group <= 0 || H % group) return DASH_ERR_INVALID;
   if (mask != DASH_MASK_FULL && mask != DASH_MASK_CAUSAL) return DASH_ERR_INVALID;
   if (!sched_known(sched)) return DASH_ERR_INVALID;
+  if (order_log && !aligned4(order_log)) return DASH_ERR_INVALID;
   // refuse before enqueuing anything: every sequence must be runnable with this schedule
   DevInfo dev;
   if ((st = device_info(&dev)) != DASH_OK) return st;
-  const int Hkv = H / group;
+  const int Hkv = H / group, causal = mask == DASH_MASK_CAUSAL;
+  const int rs_all = resolve_sched(sched, mask, D, tiles(mx), group);
+  const bool packed = mx > 0 && packed_sched(rs_all);
   for (int b = 0; b < batch; ++b) {
     const int S = cu_seqlens[b + 1] - cu_seqlens[b];
     if (S == 0) continue;
     if ((st = check_sizes(1, S, H, group, D)) != DASH_OK) return st;
+    if (packed) continue;
     const int N = tiles(S), rs = resolve_sched(sched, mask, D, N, group);
     LaunchPlan plan;
-    if (!make_plan(rs, mask == DASH_MASK_CAUSAL, N, Hkv, dev.sms, &plan))
-      return DASH_ERR_UNSUPPORTED;
+    if (!make_plan(rs, causal, N, Hkv, dev.sms, &plan)) return DASH_ERR_UNSUPPORTED;
+  }
+  if (mx == 0) return DASH_OK;
+  const void *ptrs[] = {q, k, v, o, dout, dq, dk, dv};
+  for (const void *ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return DASH_ERR_INVALID;
+  if (!lse || !aligned4(lse)) return DASH_ERR_INVALID;
+  if (!workspace || !aligned16(workspace)) return DASH_ERR_WORKSPACE;
+  // the order log is [tiles of all sequences][longest sequence's tile count]
+  const int log_stride = tiles(mx);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (packed) {
+    const size_t need = varlen_packed_bytes(cu_seqlens, batch, H, group, D, causal);
+    if (need == 0) return DASH_ERR_UNSUPPORTED;
+    if (workspace_bytes < need) return DASH_ERR_WORKSPACE;
+    const float sc = resolve_scale(scale, D);
+    size_t tiles_before = 0;
+    for (int b = 0; b < batch;) {
+      const VarlenGroup g = next_group(cu_seqlens, batch, b, H, Hkv, causal);
+      if (g.nseq > 0) {
+        st = bwd_varlen_group(g, cu_seqlens, q, k, v, o, dout, lse, dq, dk, dv, H, group, D, sc,
+                              causal, rs_all, dev.sms, workspace, s, b > 0,
+                              order_log ? order_log + tiles_before * log_stride : nullptr,
+                              log_stride);
+        if (st != DASH_OK) return st;
+      }
+      tiles_before += g.ntiles;
+      b = g.b1;
+    }
+    return DASH_OK;
   }
   if (workspace_bytes < dash_attn_bwd_workspace_bytes(1, mx, H, D)) return DASH_ERR_WORKSPACE;
   bool first = true;
+  size_t tiles_before = 0;
   for (int b = 0; b < batch; ++b) {
     const int s0 = cu_seqlens[b], S = cu_seqlens[b + 1] - s0;
     if (S == 0) continue;
@@ -454,11 +660,35 @@ dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, 
                   static_cast<const __nv_bfloat16 *>(dout) + qo, lse + (size_t)s0 * H,
                   static_cast<__nv_bfloat16 *>(dq) + qo, static_cast<__nv_bfloat16 *>(dk) + ko,
                   static_cast<__nv_bfloat16 *>(dv) + ko, 1, S, H, group, D, scale, mask, sched,
-                  workspace, workspace_bytes, DASH_BWD_ALL, stream, !first, nullptr);
+                  workspace, workspace_bytes, DASH_BWD_ALL, stream, !first,
+                  order_log ? order_log + tiles_before * log_stride : nullptr, log_stride);
     if (st != DASH_OK) return st;
     first = false;
+    tiles_before += (size_t)H * tiles(S);
   }
   return DASH_OK;
+}
+
+dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse, void *dq, void *dk,
+                                   void *dv, const int *cu_seqlens, int batch, int H, int group,
+                                   int D, float scale, dash_mask_t mask, dash_sched_t sched,
+                                   void *workspace, size_t workspace_bytes,
+                                   dash_stream_t stream) {
+  return bwd_varlen_impl(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, batch, H, group, D, scale,
+                         mask, sched, workspace, workspace_bytes, stream, nullptr);
+}
+
+dash_status_t dash_attn_bwd_varlen_order_log(const void *q, const void *k, const void *v,
+                                             const void *o, const void *dout, const float *lse,
+                                             void *dq, void *dk, void *dv, const int *cu_seqlens,
+                                             int batch, int H, int group, int D, float scale,
+                                             dash_mask_t mask, dash_sched_t sched,
+                                             void *workspace, size_t workspace_bytes,
+                                             int *order_log, dash_stream_t stream) {
+  if (!order_log) return DASH_ERR_INVALID;
+  return bwd_varlen_impl(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, batch, H, group, D, scale,
+                         mask, sched, workspace, workspace_bytes, stream, order_log);
 }
 
 dash_status_t dash_attn_status(void *workspace, dash_stream_t stream) {

@@ -31,7 +31,15 @@ struct BwdParams {
   uint32_t *status;   // status word (error bit flags)
   __nv_bfloat16 *dk;  // [B,S,Hkv,D]
   __nv_bfloat16 *dv;  // [B,S,Hkv,D]
-  int *order_log;     // optional [B,H,N,N]: rank of (q, kv) in tile q's order, as executed
+  int *order_log;     // optional [tiles][log_stride]: rank of (q, kv) in tile q's order, as
+                      // executed, at [tile (b,h,q)][kv] ([B,H,N,N] for a uniform batch)
+  int log_stride;
+  // packed variable-length batch (mode bit 3): per sequence b, seqs[b] = {S_b, first token,
+  // index of its first tile in the per-tile arrays, N_b}; seq_wprefix[b] = packed index of
+  // its first worker (batch + 1 entries); units = all sequences' workers
+  const int4 *seqs;
+  const int *seq_wprefix;
+  int batch, units;
   int B, S, H, Hkv, G, N;
   int causal;
   int heads;    // B * Hkv (b, kv head) pairs
@@ -74,12 +82,19 @@ size_t fwd_smem_bytes(int D);
 
 // mode: bits 0-1: 0 = full mask; 1 = causal mask; 2 = causal mask under Symmetric Shift
 // (shift traversal) with an odd tile count, i.e. the padded schedule; bit 2 (value 4): two
-// accumulation strands (ordered).  The tile kernel is compiled once per mode.
+// accumulation strands (ordered); bit 3 (value 8): a packed variable-length batch (3-D tensor
+// maps over the tokens, per-sequence lengths, the packed shift traversal, odd tile counts
+// read per sequence).  The tile kernel is compiled once per mode.
 // The ordered (deterministic) launch is cooperative: the runtime starts it only with every
 // CTA of the grid resident at once, so a worker never waits on a CTA that cannot start.
 cudaError_t launch_bwd(int D, bool deterministic, int mode, const CUtensorMap &tq,
                        const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tdo,
                        const BwdParams &p, int grid, cudaStream_t stream);
+// The packed variable-length launch (mode bit 3 set, the mask and the strands as given).
+cudaError_t launch_bwd_varlen(int D, bool deterministic, bool causal, bool dual,
+                              const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                              const CUtensorMap &tdo, const BwdParams &p, int grid,
+                              cudaStream_t stream);
 cudaError_t launch_fwd(int D, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
@@ -88,6 +103,24 @@ cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
 // dQ = bf16(scale * (strand 0 + ... + strand K-1)) for every row < S.
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B,
                               int S, int H, int D, int strands, cudaStream_t stream);
+
+// Packed variable-length batches: the sequence table (at most kMaxVarlenSeqs sequences) is
+// written into the workspace by a one-block kernel that receives it as its parameter.
+constexpr int kMaxVarlenSeqs = 1024;
+struct VarlenTable {
+  int4 seqs[kMaxVarlenSeqs];           // {S_b, first token, first tile, N_b}
+  int wprefix[kMaxVarlenSeqs + 1];     // packed index of sequence b's first worker
+  int batch;
+};
+cudaError_t launch_varlen_setup(const VarlenTable &t, int4 *seqs, int *wprefix,
+                                cudaStream_t stream);
+// preprocess and convert over a packed batch of T tokens (sequence table in device memory)
+cudaError_t launch_preprocess_varlen(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
+                                     const float *lse, float *dvec, float *lse2, const int4 *seqs,
+                                     int batch, int T, int H, int D, cudaStream_t stream);
+cudaError_t launch_dq_convert_varlen(const float *dqacc, __nv_bfloat16 *dq, float scale,
+                                     const int4 *seqs, int batch, int T, int H, int D,
+                                     int strands, cudaStream_t stream);
 // Strands a dQ tile's accumulation is split into (DASH_SCHED_SHIFT_DUAL: 2), at most:
 constexpr int kMaxStrands = 2;
 

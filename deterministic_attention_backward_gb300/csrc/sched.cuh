@@ -166,13 +166,17 @@ DASH_HD int shift_visit_step(int causal, int N, int kv, int q, int odd) {
   const int c = Np - 1 - kv;  // worker c, second segment (block Np-1-c)
   return (Np - c) + (Np - 1 - q);
 }
-// The phase [lo, hi) of worker w of head hd: the workers of hd in w's round.
-DASH_HD void packed_phase(int W, int P, int hd, int w, int *lo, int *hi) {
-  const long long s0 = (long long)hd * W;
+// The phase [lo, hi) of worker w of a head of W workers whose first worker has packed index
+// s0: the workers of the head in w's round.
+DASH_HD void packed_phase_at(long long s0, int W, int P, int w, int *lo, int *hi) {
   const long long round = (s0 + w) / P;
   long long a = round * P - s0, b = (round + 1) * P - s0;
   *lo = (int)(a < 0 ? 0 : a);
   *hi = (int)(b > W ? W : b);
+}
+// The same for head hd when every head has W workers (laid out head-major).
+DASH_HD void packed_phase(int W, int P, int hd, int w, int *lo, int *hi) {
+  packed_phase_at((long long)hd * W, W, P, w, lo, hi);
 }
 // Contributions to tile q from the workers [0, lo) of earlier rounds (all allowed blocks).
 DASH_HD int packed_count_before(int causal, int N, int q, int lo, int odd) {

@@ -253,13 +253,27 @@ dash_status_t dash_attn_noalloc_status(dash_stream_t stream);
  *                  starts at float offset H * cu_seqlens[b]); 4-byte aligned
  *   cu_seqlens   : HOST array of batch+1 ints, cu_seqlens[0] = 0, non-decreasing; sequence
  *                  b is tokens [cu_seqlens[b], cu_seqlens[b+1]) (S_b may be 0 or any length).
- * Each sequence is an independent attention problem (the mask applies within it) and runs
- * as the B = 1 call on its slices, one after another on `stream`, so its results -- and
- * their bit-identity under an ordered schedule -- are those of that call.  The workspace is
- * shared by the sequences: size it with dash_attn_bwd_varlen_workspace_bytes (the longest
- * sequence's need).  The backward checks every sequence against the schedule before it
- * enqueues anything (DASH_SCHED_AUTO picks per sequence); the device status word collects
- * the flags of all sequences.  Returns as the B = 1 calls do. */
+ * Each sequence is an independent attention problem (the mask applies within it).  The
+ * forward runs each sequence as the B = 1 call on its slices.  The backward:
+ *   - DASH_SCHED_SHIFT_FILL, DASH_SCHED_SHIFT_DUAL and DASH_SCHED_ATOMIC (and DASH_SCHED_AUTO,
+ *     resolved once with the longest sequence's tile count, always to one of the first two)
+ *     pack the workers of every sequence's heads onto the persistent grid in ONE tile-kernel
+ *     launch per group of at most 1024 non-empty sequences: sequence b has its own
+ *     N_b = ceil(S_b/128) tiles and, for causal masks, its own Symmetric Shift parity; the
+ *     workers of all sequences are laid out sequence-major, then kv-head-major (the order
+ *     of the uniform batch's heads) and dealt round-robin to the CTAs, so each dQ tile's
+ *     accumulation order is the packed shift order at its sequence's position in that
+ *     layout -- fixed by cu_seqlens, H, group, the mask and the SM count, hence bit-identical
+ *     from run to run, but not in general the order of the B = 1 call on the sequence alone
+ *     (equal where every head's workers fall in one round of the grid in both layouts);
+ *   - DASH_SCHED_SERIAL, DASH_SCHED_DESCENDING, DASH_SCHED_SHIFT run each sequence as the
+ *     B = 1 call on its slices, one after another on `stream`, with the results of that call.
+ * The workspace is shared by the groups or sequences: size it with
+ * dash_attn_bwd_varlen_workspace_bytes (the largest of the longest sequence's need and a
+ * packed group's need: per-tile arrays for every tile of the group plus a 20.5 KB sequence
+ * table).  The backward checks every sequence before it enqueues anything; the device
+ * status word collects the flags of all groups or sequences.  Returns as the B = 1 calls
+ * do, plus DASH_ERR_UNSUPPORTED where a packed group exceeds 2^30 tiles, tokens or workers. */
 size_t dash_attn_bwd_varlen_workspace_bytes(const int *cu_seqlens, int batch, int H, int D);
 dash_status_t dash_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
                                    float *lse, const int *cu_seqlens, int batch, int H,
@@ -272,6 +286,19 @@ dash_status_t dash_attn_bwd_varlen(const void *q, const void *k, const void *v, 
                                    int D, float scale, dash_mask_t mask, dash_sched_t sched,
                                    void *workspace, size_t workspace_bytes,
                                    dash_stream_t stream);
+/* dash_attn_bwd_varlen with the audit record of dash_attn_bwd_order_log: order_log (device,
+ * int32, 4-byte aligned, caller-owned) is [tiles][Nmax], Nmax = the longest sequence's tile
+ * count and the tiles those of the non-empty sequences in order, each [H, N_b]: entry
+ * [tile (b, h, q)][kv] receives the rank at which KV block kv's partial was added into dQ tile
+ * q of sequence b (ordered schedules; entries of pairs not visited are left unchanged).
+ * DASH_ERR_INVALID when order_log is NULL. */
+dash_status_t dash_attn_bwd_varlen_order_log(const void *q, const void *k, const void *v,
+                                             const void *o, const void *dout, const float *lse,
+                                             void *dq, void *dk, void *dv, const int *cu_seqlens,
+                                             int batch, int H, int group, int D, float scale,
+                                             dash_mask_t mask, dash_sched_t sched,
+                                             void *workspace, size_t workspace_bytes,
+                                             int *order_log, dash_stream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *dash_status_string(dash_status_t status);

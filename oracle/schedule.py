@@ -193,3 +193,30 @@ def packed_reduction_order(sched: str, causal: bool, N: int, heads: int, P: int)
         assert len(set(times)) == len(times), "two contributions to one tile at one time"
         out[key] = [kv for _, kv in a]
     return out
+
+
+# A packed batch of heads with different tile counts (variable-length sequences): head i has
+# Ns[i] tiles and its own shift workers; the workers of all heads are laid out one after
+# another in the given head order and dealt round-robin to P processors as above.  The pages
+# treat one length at a time; the reading taken is that every head keeps the shift order of
+# its own length and the accumulation order of its tiles is again the time order of their
+# contributions.  Only contributions of one head are ever compared, so the time of a
+# contribution is its (round, step) pair.
+def packed_reduction_order_mixed(sched: str, causal: bool, Ns: list[int], P: int):
+    """(head, q) -> KV blocks in the order their partials are added, head i of Ns[i] tiles."""
+    arrivals: dict = {}
+    base = 0
+    for hd, N in enumerate(Ns):
+        W = num_workers(sched, causal, N)
+        for w in range(W):
+            rnd = (base + w) // P
+            for t, kv, q in timed_visits(sched, causal, N, w):
+                arrivals.setdefault((hd, q), []).append(((rnd, t), kv))
+        base += W
+    out = {}
+    for key, a in arrivals.items():
+        a.sort()
+        times = [t for t, _ in a]
+        assert len(set(times)) == len(times), "two contributions to one tile at one time"
+        out[key] = [kv for _, kv in a]
+    return out

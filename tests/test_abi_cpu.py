@@ -183,13 +183,19 @@ def test_auto_schedule_resolution(L, causal, N, D):
 
 def test_varlen_arguments_and_workspace(L):
     """Packed-batch entry points: offsets are checked before anything runs, and the shared
-    workspace is the longest sequence's need."""
+    workspace is the packed launch's need (per-tile arrays for every tile of the batch plus
+    the 1024-entry sequence table: 16 bytes and 4 bytes per entry, each part 256-aligned),
+    at least the longest sequence's."""
     import ctypes as ct
     arr = lambda xs: (ct.c_int * len(xs))(*xs)
     fake = 1 << 20
     cu = arr([0, 200, 712, 749])
+    table = 16 * 1024 + (4 * 1025 + 255) // 256 * 256
+    # 2 + 4 + 1 tiles per head, 4 heads: the arrays of 7 tiles of a B = 1 call
     assert L.dash_attn_bwd_varlen_workspace_bytes(cu, 3, 4, 64) == \
-        dash.bwd_workspace_bytes(1, 512, 4, 64)
+        dash.bwd_workspace_bytes(1, 7 * 128, 4, 64) + table
+    assert L.dash_attn_bwd_varlen_workspace_bytes(arr([0, 0, 300, 300]), 3, 2, 128) == \
+        dash.bwd_workspace_bytes(1, 300, 2, 128) + table
     assert L.dash_attn_bwd_varlen_workspace_bytes(arr([0, 5, 3]), 2, 4, 64) == 0   # decreasing
     assert L.dash_attn_bwd_varlen_workspace_bytes(arr([1, 5]), 1, 4, 64) == 0      # cu[0] != 0
     args = [fake] * 9
@@ -200,6 +206,9 @@ def test_varlen_arguments_and_workspace(L):
     assert L.dash_attn_bwd_varlen(*args, cu, 3, 4, 1, 64, 0.0, 0, 7, fake, 1 << 30, None) == 1
     assert L.dash_attn_fwd_varlen(*([fake] * 5), arr([2, 4]), 1, 4, 1, 64, 0.0, 0, fake, 256,
                                   None) == 1
+    # the audit form wants its log
+    assert L.dash_attn_bwd_varlen_order_log(*args, cu, 3, 4, 1, 64, 0.0, 0, 4, fake, 1 << 30,
+                                            None, None) == 1
 
 
 def test_wait_limit_setting(L):

@@ -140,3 +140,33 @@ def test_packed_shift_is_conflict_free_and_reduces_to_shift(causal, N, heads, P)
         if len({rounds[(hd, w)] for w in range(W)}) == 1:     # a head inside one round
             plain = sc.reduction_order(sched, causal, N)
             assert all(order[(hd, q)] == plain[q] for q in range(N))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Ns,P", [([2, 4, 1, 9], 7), ([8] * 5, 12), ([3, 16, 5, 1, 1, 7, 12], 10),
+                                  ([32, 2, 31], 38), ([1] * 9, 4)])
+def test_mixed_packing_keeps_each_heads_shift_order(causal, Ns, P):
+    """Heads of different lengths packed together: every tile's order is a permutation of its
+    allowed blocks, a head inside one round keeps its plain shift order, and a head's order
+    depends only on where its workers fall in the rounds -- equal lengths give the uniform
+    packing's order exactly."""
+    sched = sc.SYMSHIFT if causal else sc.SHIFT
+    order = sc.packed_reduction_order_mixed(sched, causal, Ns, P)
+    base = 0
+    for hd, N in enumerate(Ns):
+        W = sc.num_workers(sched, causal, N)
+        for q in range(N):
+            assert sorted(order[(hd, q)]) == [kv for kv in range(N) if sc.allowed(causal, q, kv)]
+        if base // P == (base + W - 1) // P:
+            plain = sc.reduction_order(sched, causal, N)
+            assert all(order[(hd, q)] == plain[q] for q in range(N))
+        # the same head alone, at the same offset within a round (padding heads of 1 tile
+        # in front shift it there): the order depends on nothing else
+        pad = base % P
+        alone = sc.packed_reduction_order_mixed(sched, causal, [1] * pad + [N], P)
+        assert sc.num_workers(sched, causal, 1) == 1
+        assert all(alone[(pad, q)] == order[(hd, q)] for q in range(N))
+        base += W
+    if len(set(Ns)) == 1:
+        uni = sc.packed_reduction_order(sched, causal, Ns[0], len(Ns), P)
+        assert uni == order
