@@ -166,9 +166,9 @@ bool sched_known(int sched) {
 // DASH_SCHED_SHIFT_DUAL shares.
 int resolve_sched(int sched, int mask, int D, int N, int G) {
   if (sched != DASH_SCHED_AUTO) return sched;
-  if (N < 8) return DASH_SCHED_SHIFT_FILL;
-  if (mask == DASH_MASK_FULL) return DASH_SCHED_SHIFT_DUAL;
-  if (D == 128 && (G > 1 || N >= 64)) return DASH_SCHED_SHIFT_DUAL;
+  (void)N;
+  (void)G;
+  if (mask == DASH_MASK_FULL || D == 128) return DASH_SCHED_SHIFT_DUAL;
   return DASH_SCHED_SHIFT_FILL;
 }
 
@@ -291,10 +291,11 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
   const BwdWorkspace w = carve_bwd(workspace, B, S, H, D);
   const float sc = resolve_scale(scale, D);
   if (stages & DASH_BWD_PROLOGUE) {
-    // status word and semaphores are contiguous; the accumulator separately
+    // status word and semaphores are contiguous; the accumulator is cleared unless it has
+    // two strands (SHIFT_DUAL stores the first partial of each strand)
     if ((keep_status ? cudaMemsetAsync(w.sem, 0, w.sem_bytes, s)
                      : cudaMemsetAsync(w.status, 0, kStatusBytes + w.sem_bytes, s)) != cudaSuccess ||
-        cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes * K, s) != cudaSuccess)
+        (K == 1 && cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes, s) != cudaSuccess))
       return DASH_ERR_CUDA;
     // a partial last tile: its padding rows of lse2 / Dvec must read as zero
     if ((S % kTile) &&
@@ -345,8 +346,8 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
                        tq, tk, tv, tdo, p, plan.grid, s) != cudaSuccess)
     return DASH_ERR_CUDA;
   if ((stages & DASH_BWD_EPILOGUE) &&
-      dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, K, s) !=
-          cudaSuccess)
+      dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, K, causal,
+                              s) != cudaSuccess)
     return DASH_ERR_CUDA;
   return DASH_OK;
 }
@@ -542,7 +543,7 @@ static dash_status_t bwd_varlen_group(const VarlenGroup &g, const int *cu, const
     return DASH_ERR_CUDA;
   if ((keep_status ? cudaMemsetAsync(w.sem, 0, w.sem_bytes, s)
                    : cudaMemsetAsync(w.status, 0, kStatusBytes + w.sem_bytes, s)) != cudaSuccess ||
-      cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes * K, s) != cudaSuccess)
+      (K == 1 && cudaMemsetAsync(w.dqacc, 0, w.dqacc_bytes, s) != cudaSuccess))
     return DASH_ERR_CUDA;
   if (g.ragged &&
       cudaMemsetAsync(w.lse2, 0, reinterpret_cast<char *>(w.dqacc) - reinterpret_cast<char *>(w.lse2),
@@ -584,7 +585,7 @@ static dash_status_t bwd_varlen_group(const VarlenGroup &g, const int *cu, const
   if (dash::launch_bwd_varlen(D, ordered, causal, K > 1, tq, tk, tv, tdo, p, grid, s) !=
           cudaSuccess ||
       dash::launch_dq_convert_varlen(w.dqacc, static_cast<bf *>(dq) + qo, sc, seqs, n, T, H, D,
-                                     K, s) != cudaSuccess)
+                                     K, causal, s) != cudaSuccess)
     return DASH_ERR_CUDA;
   return DASH_OK;
 }

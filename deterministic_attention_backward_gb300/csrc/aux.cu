@@ -75,7 +75,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16 *__
 template <int D, int K>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
                                                          __nv_bfloat16 *__restrict__ dq,
-                                                         float scale, int B, int S, int H) {
+                                                         float scale, int B, int S, int H,
+                                                         int causal) {
   constexpr int C4 = D / 4;
   const int N = (S + kTile - 1) / kTile;
   const long long total = (long long)B * H * N * kTile * C4;
@@ -91,9 +92,11 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
     if (i * kTile + r >= S) continue;  // padding rows of a partial last tile
     const float *tb = acc + t * K * (C4 * kTile * 4);
     float4 v = *reinterpret_cast<const float4 *>(tb + ((size_t)c4 * kTile + r) * 4);
-    if constexpr (K == 2) {  // strand 0 + strand 1
-      const float4 w = *reinterpret_cast<const float4 *>(tb + ((size_t)(C4 + c4) * kTile + r) * 4);
-      v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+    if constexpr (K == 2) {  // strand 0 + strand 1 (when the tile has a second partial)
+      if ((causal ? i + 1 : N) > 1) {
+        const float4 w = *reinterpret_cast<const float4 *>(tb + ((size_t)(C4 + c4) * kTile + r) * 4);
+        v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+      }
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
     __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(256) preprocess_varlen_kernel(
 template <int D, int K>
 __global__ void __launch_bounds__(256) dq_convert_varlen_kernel(
     const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, float scale,
-    const int4 *__restrict__ seqs, int batch, int T, int H) {
+    const int4 *__restrict__ seqs, int batch, int T, int H, int causal) {
   constexpr int C4 = D / 4;
   const long long total = (long long)T * H * C4;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -166,8 +169,10 @@ __global__ void __launch_bounds__(256) dq_convert_varlen_kernel(
     const float *tb = acc + tile * K * (C4 * kTile * 4);
     float4 v = *reinterpret_cast<const float4 *>(tb + ((size_t)c4 * kTile + r) * 4);
     if constexpr (K == 2) {
-      const float4 w = *reinterpret_cast<const float4 *>(tb + ((size_t)(C4 + c4) * kTile + r) * 4);
-      v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+      if ((causal ? i / kTile + 1 : sq.w) > 1) {
+        const float4 w = *reinterpret_cast<const float4 *>(tb + ((size_t)(C4 + c4) * kTile + r) * 4);
+        v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+      }
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
     __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
@@ -199,19 +204,19 @@ cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
 }
 
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B, int S,
-                              int H, int D, int strands, cudaStream_t stream) {
+                              int H, int D, int strands, int causal, cudaStream_t stream) {
   const long long work = (long long)B * H * ((S + kTile - 1) / kTile) * kTile * (D / 4);
   const int grid = grid_for(work, 256, 152 * 32);
   if (D == 64) {
     if (strands == 2)
-      dq_convert_kernel<64, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+      dq_convert_kernel<64, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
     else
-      dq_convert_kernel<64, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+      dq_convert_kernel<64, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
   } else {
     if (strands == 2)
-      dq_convert_kernel<128, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+      dq_convert_kernel<128, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
     else
-      dq_convert_kernel<128, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H);
+      dq_convert_kernel<128, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
   }
   return cudaGetLastError();
 }
@@ -238,21 +243,21 @@ cudaError_t launch_preprocess_varlen(const __nv_bfloat16 *o, const __nv_bfloat16
 
 cudaError_t launch_dq_convert_varlen(const float *dqacc, __nv_bfloat16 *dq, float scale,
                                      const int4 *seqs, int batch, int T, int H, int D,
-                                     int strands, cudaStream_t stream) {
+                                     int strands, int causal, cudaStream_t stream) {
   const long long work = (long long)T * H * (D / 4);
   const int grid = grid_for(work, 256, 152 * 32);
   if (D == 64) {
     if (strands == 2)
-      dq_convert_varlen_kernel<64, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T, H);
+      dq_convert_varlen_kernel<64, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T, H, causal);
     else
-      dq_convert_varlen_kernel<64, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T, H);
+      dq_convert_varlen_kernel<64, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T, H, causal);
   } else {
     if (strands == 2)
       dq_convert_varlen_kernel<128, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T,
-                                                                 H);
+                                                                 H, causal);
     else
       dq_convert_varlen_kernel<128, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T,
-                                                                 H);
+                                                                 H, causal);
   }
   return cudaGetLastError();
 }

@@ -704,7 +704,7 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
             ok = ok && sem_wait(sem, want, ab) ? 1 : 0;
             DASH_TRACE(p, 30);
             if (ok) {
-              if constexpr (kDual) ranks[slot] = rank;
+              ranks[slot] = rank;
               mbar_arrive(&bar.turn_full[slot]);
             }
             // audit record of the executed order (dash_attn_bwd_order_log)
@@ -760,6 +760,15 @@ __device__ void bwd_releaser(const BwdParams &p, uint8_t *smem, const Bars<D, DE
   }
 }
 
+// What the epilogue learns with its turn (ordered modes), from the partial's rank in its dQ
+// tile: 1 + its strand (rank mod 2 with two strands, else 0) + 2 if it is its strand's first
+// partial (rank < strands; used with two strands).  0 stands for a failed wait.
+template <bool kDual>
+__device__ __forceinline__ int turn_code(int rank) {
+  constexpr int K = kDual ? 2 : 1;
+  return 1 + (kDual ? (rank & 1) : 0) + (rank < K ? 2 : 0);
+}
+
 template <int D, bool DET, int MODE>
 __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
                              const Abort &ab) {
@@ -804,7 +813,7 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
             g5 = mbar_wait(bar.g5_done, it & 1, ab) ? 1 : 0;
             if (kDual && g5)
               g5 = mbar_wait(&bar.turn_full[it % L::kTurns], (it / L::kTurns) & 1, ab)
-                       ? 1 + (ranks[it % L::kTurns] & 1)
+                       ? turn_code<kDual>(ranks[it % L::kTurns])
                        : 0;
           }
           g5 = agree_int(g5);
@@ -854,7 +863,9 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
           int turn = g5;
           if constexpr (DET && !kDual) {
             if (et == 0) {
-              turn = mbar_wait(&bar.turn_full[it % L::kTurns], (it / L::kTurns) & 1, ab) ? 1 : 0;
+              turn = mbar_wait(&bar.turn_full[it % L::kTurns], (it / L::kTurns) & 1, ab)
+                         ? turn_code<kDual>(ranks[it % L::kTurns])
+                         : 0;
               DASH_TRACE(p, 28);
             }
             turn = agree_int(turn);
@@ -863,21 +874,34 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
             ok = false;
             break;
           }
-          const size_t acc_idx = kDual ? tile_idx * 2 + (turn - 1) : tile_idx;
+          // two strands: the first partial of a strand is stored, so their accumulator needs
+          // no clearing beforehand (measured: +12 % for the whole call at S = 512, neutral at
+          // 16k; with one strand the second copy of the unrolled loop cost 3-5 % at long S,
+          // so there the accumulator is cleared and every partial added)
+          const bool first = kDual && ((turn - 1) >> 1) != 0;
+          const size_t acc_idx = kDual ? tile_idx * 2 + ((turn - 1) & 1) : tile_idx;
           float *tile = p.dqacc + acc_idx * (size_t)(kTile * D);
           if (et == 0) DASH_TRACE(p, 16);
+          // one branch per step (a branch per vector inside the unrolled loop cost 4-7 %:
+          // the epilogue shares its SMSPs with the issue-bound softmax-gradient warps)
+          auto out_partial = [&](auto op) {
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
+            for (int ch = 0; ch < D / 32; ++ch) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int c4 = ch * 8 + j;
-              red_add_v4(tile + ((size_t)c4 * kTile + r) * 4, __uint_as_float(v[ch][4 * j]),
-                         __uint_as_float(v[ch][4 * j + 1]), __uint_as_float(v[ch][4 * j + 2]),
-                         __uint_as_float(v[ch][4 * j + 3]));
-              if ((!DET || kDual) && (ch * 8 + j + 1) % kRedPaceEvery == 0 && ch * 8 + j + 1 < D / 4)
-                __nanosleep(kRedPaceNs);
+              for (int j = 0; j < 8; ++j) {
+                const int c4 = ch * 8 + j;
+                op(tile + ((size_t)c4 * kTile + r) * 4, __uint_as_float(v[ch][4 * j]),
+                   __uint_as_float(v[ch][4 * j + 1]), __uint_as_float(v[ch][4 * j + 2]),
+                   __uint_as_float(v[ch][4 * j + 3]));
+                if ((!DET || kDual) && (c4 + 1) % kRedPaceEvery == 0 && c4 + 1 < D / 4)
+                  __nanosleep(kRedPaceNs);
+              }
             }
-          }
+          };
+          if (first)
+            out_partial([](float *d, float a, float b, float c, float e) { st_v4(d, a, b, c, e); });
+          else
+            out_partial([](float *d, float a, float b, float c, float e) { red_add_v4(d, a, b, c, e); });
           if constexpr (kDual) {  // each warp's reductions issued: the releaser releases
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.added[it % L::kTurns]);

@@ -27,6 +27,7 @@ struct BwdParams {
   const float *lse2;  // [B,H,N*128]  LSE * log2(e)
   const float *dvec;  // [B,H,N*128]  rowsum(dO * O)
   float *dqacc;       // fp32 dQ accumulator, tile-native [B,H,N][K][D/4][128][4], K strands
+                      // (two strands: a strand's first partial is stored, no clearing needed)
   int *sem;           // [B,H,N][K] ordering semaphores (partials added so far, per strand)
   uint32_t *status;   // status word (error bit flags)
   __nv_bfloat16 *dk;  // [B,S,Hkv,D]
@@ -100,9 +101,12 @@ cudaError_t launch_fwd(int D, const CUtensorMap &tq, const CUtensorMap &tk,
 cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
                               const float *lse, float *dvec, float *lse2, int B, int S, int H,
                               int D, cudaStream_t stream);
-// dQ = bf16(scale * (strand 0 + ... + strand K-1)) for every row < S.
+// dQ = bf16(scale * (strand 0 + ... + strand K-1)) for every row < S.  A strand s that
+// received no partial (a tile with s or fewer: query tile 0 of a causal mask, or N = 1) is
+// not read: the two-strand schedule stores each strand's first partial instead of clearing
+// the accumulator.
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B,
-                              int S, int H, int D, int strands, cudaStream_t stream);
+                              int S, int H, int D, int strands, int causal, cudaStream_t stream);
 
 // Packed variable-length batches: the sequence table (at most kMaxVarlenSeqs sequences) is
 // written into the workspace by a one-block kernel that receives it as its parameter.
@@ -120,7 +124,7 @@ cudaError_t launch_preprocess_varlen(const __nv_bfloat16 *o, const __nv_bfloat16
                                      int batch, int T, int H, int D, cudaStream_t stream);
 cudaError_t launch_dq_convert_varlen(const float *dqacc, __nv_bfloat16 *dq, float scale,
                                      const int4 *seqs, int batch, int T, int H, int D,
-                                     int strands, cudaStream_t stream);
+                                     int strands, int causal, cudaStream_t stream);
 // Strands a dQ tile's accumulation is split into (DASH_SCHED_SHIFT_DUAL: 2), at most:
 constexpr int kMaxStrands = 2;
 

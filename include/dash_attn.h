@@ -91,15 +91,16 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *  DASH_SCHED_AUTO       -- the deterministic schedule that measured fastest on GB300 for
  *                           the mask, head dim, tile count N and group size G
  *                           (dash_sched_resolve names it): the pages leave the choice to the
- *                           user.  Table, from the benchmark's whole-call timings (full mask
- *                           H16 and causal H32 at D = 128 and 64, S = 512 .. 16384, GQA 4:1):
- *                             N < 8                               -> SHIFT_FILL
- *                             full mask                           -> SHIFT_DUAL (D = 128:
- *                                                                    +5 % at N = 8, +16 % at
- *                                                                    N = 128; D = 64: +12 %)
- *                             D = 128, causal, G > 1              -> SHIFT_DUAL (+8 %, N = 64)
- *                             D = 128, causal, G = 1, N >= 64     -> SHIFT_DUAL (+0.5-3 %)
- *                             otherwise (causal)                  -> SHIFT_FILL (2-10 % ahead)
+ *                           user.  Table, from whole-call timings (full mask H16 and causal
+ *                           H32 at D = 128 and 64, S = 512 .. 16384, GQA 4:1; N and G did not
+ *                           change the winner):
+ *                             full mask                           -> SHIFT_DUAL (D = 128: +12 %
+ *                                                                    at N = 4, +16 % at N = 128;
+ *                                                                    D = 64: +11 % at N = 4)
+ *                             causal, D = 128                     -> SHIFT_DUAL (+1-3 % at
+ *                                                                    N = 4..16, +8 % GQA N = 64)
+ *                             causal, D = 64                      -> SHIFT_FILL (+1-12 %; equal
+ *                                                                    at N = 4)
  *  DASH_SCHED_SHIFT_DUAL -- packed Shift Scheduling (the SHIFT_FILL traversal, grid and ranks)
  *                           with each dQ tile accumulated in two strands: the partial of rank
  *                           r is added into strand r mod 2 as that strand's (r div 2)-th
@@ -150,12 +151,14 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
 size_t dash_attn_bwd_workspace_bytes(int B, int S, int H, int D);
 
 /* Backward pass (the DASH hot path): given Q, K, V, O, dO and LSE, writes dQ, dK, dV.
- *   Steps, all on `stream`: clear the workspace; D_i = rowsum(dO_i * O_i); the tile
- *   kernel -- per KV block, dK/dV accumulate in tensor memory on one SM while every
+ *   Steps, all on `stream`: clear the status word and the semaphores (and, unless the
+ *   schedule is DASH_SCHED_SHIFT_DUAL, the accumulator); D_i = rowsum(dO_i * O_i); the
+ *   tile kernel -- per KV block, dK/dV accumulate in tensor memory on one SM while every
  *   visited query tile's dQ partial is added to an fp32 accumulator in global memory in
  *   the order the schedule fixes, enforced by one ordering semaphore per dQ tile
  *   (section 2.1: one KV tile's operations stay on one SM; section 1: fixed dQ
- *   accumulation order); finally dQ = bf16(scale * accumulator).
+ *   accumulation order; under DASH_SCHED_SHIFT_DUAL the first partial of each strand is
+ *   stored rather than added); finally dQ = bf16(scale * accumulator).
  *   For group > 1, dK/dV of a KV head sum the group's query heads in ascending order.
  *   Deterministic schedules give bit-identical dQ/dK/dV on every run, for any grid size
  *   and under concurrent load; DASH_SCHED_ATOMIC does not.
@@ -172,7 +175,8 @@ dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const v
                             size_t workspace_bytes, dash_stream_t stream);
 
 /* The same backward in separately launchable stages, for callers that time or overlap
- * them: DASH_BWD_PROLOGUE clears the workspace and computes the row vectors
+ * them: DASH_BWD_PROLOGUE clears the workspace's status word and semaphores (and the
+ * accumulator, except under DASH_SCHED_SHIFT_DUAL) and computes the row vectors
  * (rowsum(dO*O), LSE*log2 e); DASH_BWD_TILES runs the tile kernel (the five contractions
  * and the ordered dQ reduction, dK/dV written); DASH_BWD_EPILOGUE converts the dQ
  * accumulator to bf16.  Arguments as dash_attn_bwd; stages given in separate calls must

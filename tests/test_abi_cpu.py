@@ -153,11 +153,7 @@ def test_schedule_query_rejects_bad_arguments(L):
 
 def auto_table(causal, D, N, G):
     """The measured table the header documents for DASH_SCHED_AUTO."""
-    if N < 8:
-        return "shift_fill"
-    if not causal:
-        return "shift_dual"
-    if D == 128 and (G > 1 or N >= 64):
+    if not causal or D == 128:
         return "shift_dual"
     return "shift_fill"
 
