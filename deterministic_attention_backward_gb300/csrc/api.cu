@@ -584,8 +584,8 @@ static dash_status_t bwd_varlen_group(const VarlenGroup &g, const int *cu, const
   const int grid = unit < sms ? unit : sms;
   if (dash::launch_bwd_varlen(D, ordered, causal, K > 1, tq, tk, tv, tdo, p, grid, s) !=
           cudaSuccess ||
-      dash::launch_dq_convert_varlen(w.dqacc, static_cast<bf *>(dq) + qo, sc, seqs, n, T, H, D,
-                                     K, causal, s) != cudaSuccess)
+      dash::launch_dq_convert_varlen(w.dqacc, static_cast<bf *>(dq) + qo, sc, seqs, n,
+                                     (int)g.ntiles, H, D, K, causal, s) != cudaSuccess)
     return DASH_ERR_CUDA;
   return DASH_OK;
 }

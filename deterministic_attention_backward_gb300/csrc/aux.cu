@@ -13,38 +13,52 @@
 namespace dash {
 namespace {
 
-// sum_d o[d] * dout[d] over one D-element row, by one warp (every lane gets the sum).
-template <int D>
-__device__ __forceinline__ float row_dot(const __nv_bfloat16 *__restrict__ o,
-                                         const __nv_bfloat16 *__restrict__ dout, int lane) {
-  constexpr int kPer = D / 32;  // bf16 elements per lane (2 or 4)
-  const __nv_bfloat16 *po = o + lane * kPer;
-  const __nv_bfloat16 *pd = dout + lane * kPer;
-  float acc = 0.f;
-  if constexpr (kPer == 4) {
-    const uint2 a = *reinterpret_cast<const uint2 *>(po);
-    const uint2 c = *reinterpret_cast<const uint2 *>(pd);
-    const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
-    const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&c);
+// Dot products sum_d o[d] * dout[d] of `rows` consecutive D-element rows: L = D/8 lanes per
+// row, 16 bytes each, U groups of 32/L rows per warp per iteration with every load issued
+// before any reduction (U x 32 bytes in flight per lane: the kernel is bound by how many
+// loads it keeps in flight); fn(row, dot) runs on the row's first lane.  O is read once
+// (streaming loads); dO stays cacheable for the tile kernel that reads it next.
+template <int D, typename F>
+__device__ __forceinline__ void for_each_row_dot(const __nv_bfloat16 *__restrict__ o,
+                                                 const __nv_bfloat16 *__restrict__ dout,
+                                                 long long rows, F fn) {
+  constexpr int L = D / 8, RPW = 32 / L, U = 4;
+  const int lane = threadIdx.x & 31, sub = lane / L, li = lane % L;
+  const long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long base = w * (RPW * U); base < rows; base += nw * (RPW * U)) {
+    uint4 a[U], c[U];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(c2[e]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
+    for (int u = 0; u < U; ++u) {
+      const long long row = base + u * RPW + sub;
+      if (row < rows) {
+        a[u] = __ldcs(reinterpret_cast<const uint4 *>(o + row * D) + li);
+        c[u] = __ldg(reinterpret_cast<const uint4 *>(dout + row * D) + li);
+      } else {
+        a[u] = c[u] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
-  } else {
-    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(po));
-    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(pd));
-    acc = fmaf(x.x, y.x, acc);
-    acc = fmaf(x.y, y.y, acc);
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  return acc;
+    for (int u = 0; u < U; ++u) {
+      const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a[u]);
+      const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&c[u]);
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(c2[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+#pragma unroll
+      for (int off = L / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const long long row = base + u * RPW + sub;
+      if (li == 0 && row < rows) fn(row, acc);
+    }
+  }
 }
+constexpr int kPreRowsPerBlock = 8 * 4 * 4;  // 8 warps x U x (32 / L) at D = 64 (an upper bound)
 
-// One warp per (b, i, h) row; rows enumerated in BSHD order so the O/dO reads of a CTA are
-// one contiguous range.
+// Rows enumerated in BSHD order, so the O/dO reads of a warp are one contiguous range.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16 *__restrict__ o,
                                                          const __nv_bfloat16 *__restrict__ dout,
@@ -53,30 +67,72 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16 *__
                                                          float *__restrict__ lse2, int B, int S,
                                                          int H) {
   const long long rows = (long long)B * S * H;
-  const int lane = threadIdx.x & 31;
-  for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows;
-       row += (long long)gridDim.x * 8) {
-    const float acc = row_dot<D>(o + row * D, dout + row * D, lane);
-    if (lane == 0) {
-      const int h = (int)(row % H);
-      const long long bi = row / H;
-      const int i = (int)(bi % S);
-      const int b = (int)(bi / S);
-      const size_t Sp = (size_t)(S + kTile - 1) / kTile * kTile;
-      const size_t r = ((size_t)b * H + h) * Sp + i;
-      dvec[r] = acc;
-      lse2[r] = lse[((size_t)b * H + h) * S + i] * kLog2e;
+  for_each_row_dot<D>(o, dout, rows, [&](long long row, float acc) {
+    const int h = (int)(row % H);
+    const long long bi = row / H;
+    const int i = (int)(bi % S);
+    const int b = (int)(bi / S);
+    const size_t Sp = (size_t)(S + kTile - 1) / kTile * kTile;
+    const size_t r = ((size_t)b * H + h) * Sp + i;
+    dvec[r] = acc;
+    lse2[r] = lse[((size_t)b * H + h) * S + i] * kLog2e;
+  });
+}
+
+// dQ convert, one CTA per dQ tile: the tile's strands are read in their tile-native layout
+// ([D/4][128][4] fp32: consecutive threads take consecutive rows, 512 contiguous bytes per
+// warp), summed, scaled and rounded to bf16 into a [128][D] shared-memory tile, which is
+// then written row by row (D*2 contiguous bytes per row) -- both sides coalesced.
+template <int D>
+struct ConvTile {
+  static constexpr int kRowBytes = D * 2 + 8;  // padded: the 8-byte stores of a warp hit
+                                               // at most two rows per bank
+  static constexpr int kBytes = kTile * kRowBytes;
+};
+// Sums `strands` strands of the tile at `tb` into shared memory `st` (bf16, scaled).
+template <int D, int K>
+__device__ __forceinline__ void conv_tile_load(const float *__restrict__ tb, int strands,
+                                               float scale, uint8_t *st) {
+  constexpr int C4 = D / 4;
+  constexpr int kStrand = C4 * kTile;  // float4 per strand
+  const float4 *src = reinterpret_cast<const float4 *>(tb);
+  for (int idx = threadIdx.x; idx < kStrand; idx += blockDim.x) {
+    float4 v = __ldcs(src + idx);
+    if constexpr (K == 2) {
+      if (strands > 1) {
+        const float4 w = __ldcs(src + kStrand + idx);
+        v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+      }
     }
+    const int c4 = idx / kTile, r = idx % kTile;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t *>(&lo);
+    packed.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(st + r * ConvTile<D>::kRowBytes + c4 * 8) = packed;
+  }
+}
+// Writes rows [0, rows) of the shared tile; row r goes to dst + r * row_stride (elements).
+template <int D>
+__device__ __forceinline__ void conv_tile_store(const uint8_t *st, __nv_bfloat16 *dst,
+                                                size_t row_stride, int rows) {
+  constexpr int kPer = D / 4;  // 8-byte chunks per row
+  for (int idx = threadIdx.x; idx < rows * kPer; idx += blockDim.x) {
+    const int r = idx / kPer, c = idx % kPer;
+    *reinterpret_cast<uint2 *>(dst + (size_t)r * row_stride + c * 4) =
+        *reinterpret_cast<const uint2 *>(st + r * ConvTile<D>::kRowBytes + c * 8);
   }
 }
 
-// One thread per 4 output elements; the 4-column chunk index runs fastest so a warp
-// writes contiguous bf16 rows.  dQacc layout: [B,H,N][K][D/4][128][4], K strands.
-template <int D, int K>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
-                                                         __nv_bfloat16 *__restrict__ dq,
-                                                         float scale, int B, int S, int H,
-                                                         int causal) {
+// Two strands: one thread per 4 output elements, the 4-column chunk fastest so a warp
+// writes contiguous bf16 rows (measured faster than the per-tile form when both strands are
+// read: 77 vs 81 us for 16k tokens x 16 heads at D = 128).
+template <int D>
+__global__ void __launch_bounds__(256) dq_convert2_kernel(const float *__restrict__ acc,
+                                                          __nv_bfloat16 *__restrict__ dq,
+                                                          float scale, int B, int S, int H,
+                                                          int causal) {
   constexpr int C4 = D / 4;
   const int N = (S + kTile - 1) / kTile;
   const long long total = (long long)B * H * N * kTile * C4;
@@ -90,13 +146,11 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
     const int h = (int)(bh % H);
     const int b = (int)(bh / H);
     if (i * kTile + r >= S) continue;  // padding rows of a partial last tile
-    const float *tb = acc + t * K * (C4 * kTile * 4);
+    const float *tb = acc + t * 2 * (C4 * kTile * 4);
     float4 v = *reinterpret_cast<const float4 *>(tb + ((size_t)c4 * kTile + r) * 4);
-    if constexpr (K == 2) {  // strand 0 + strand 1 (when the tile has a second partial)
-      if ((causal ? i + 1 : N) > 1) {
-        const float4 w = *reinterpret_cast<const float4 *>(tb + ((size_t)(C4 + c4) * kTile + r) * 4);
-        v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
-      }
+    if ((causal ? i + 1 : N) > 1) {  // strand 1, when the tile has a second partial
+      const float4 w = *reinterpret_cast<const float4 *>(tb + ((size_t)(C4 + c4) * kTile + r) * 4);
+      v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
     __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
@@ -106,6 +160,27 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
     *reinterpret_cast<uint2 *>(dq + (((size_t)b * S + (size_t)i * kTile + r) * H + h) * D +
                                4 * c4) = packed;
   }
+}
+
+template <int D, int K>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
+                                                         __nv_bfloat16 *__restrict__ dq,
+                                                         float scale, int B, int S, int H,
+                                                         int causal) {
+  __shared__ __align__(16) uint8_t st[ConvTile<D>::kBytes];
+  const int N = (S + kTile - 1) / kTile;
+  const long long t = blockIdx.x;  // (b*H + h)*N + i
+  const int i = (int)(t % N);
+  const long long bh = t / N;
+  const int h = (int)(bh % H);
+  const int b = (int)(bh / H);
+  // a strand that received no partial is not read (tile with a single partial)
+  conv_tile_load<D, K>(acc + t * K * (size_t)(kTile * D), (causal ? i + 1 : N) > 1 ? K : 1,
+                       scale, st);
+  __syncthreads();
+  const int rows = S - i * kTile < kTile ? S - i * kTile : kTile;
+  conv_tile_store<D>(st, dq + (((size_t)b * S + (size_t)i * kTile) * H + h) * D,
+                     (size_t)H * D, rows);
 }
 
 // The sequence holding packed token t: the last table entry whose first token is <= t.
@@ -126,61 +201,48 @@ __global__ void varlen_setup_kernel(const VarlenTable t, int4 *__restrict__ seqs
   for (int i = threadIdx.x; i <= t.batch; i += blockDim.x) wprefix[i] = t.wprefix[i];
 }
 
-// One warp per packed (t, h) row, as preprocess_kernel.
+// The same over the packed (t, h) rows of a variable-length batch.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_varlen_kernel(
     const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
     const float *__restrict__ lse, float *__restrict__ dvec, float *__restrict__ lse2,
     const int4 *__restrict__ seqs, int batch, int T, int H) {
   const long long rows = (long long)T * H;
-  const int lane = threadIdx.x & 31;
-  for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows;
-       row += (long long)gridDim.x * 8) {
-    const float acc = row_dot<D>(o + row * D, dout + row * D, lane);
-    if (lane == 0) {
-      const int h = (int)(row % H);
-      const int t = (int)(row / H);
-      const int4 sq = seqs[seq_of_token(seqs, batch, t)];
-      const int i = t - sq.y;
-      const size_t r = ((size_t)sq.z + (size_t)h * sq.w) * kTile + i;
-      dvec[r] = acc;
-      lse2[r] = lse[(size_t)sq.y * H + (size_t)h * sq.x + i] * kLog2e;
-    }
-  }
-}
-
-// One thread per 4 output elements of a packed (t, h) row, the chunk index fastest.
-template <int D, int K>
-__global__ void __launch_bounds__(256) dq_convert_varlen_kernel(
-    const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, float scale,
-    const int4 *__restrict__ seqs, int batch, int T, int H, int causal) {
-  constexpr int C4 = D / 4;
-  const long long total = (long long)T * H * C4;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int c4 = (int)(idx % C4);
-    const long long row = idx / C4;
+  for_each_row_dot<D>(o, dout, rows, [&](long long row, float acc) {
     const int h = (int)(row % H);
     const int t = (int)(row / H);
     const int4 sq = seqs[seq_of_token(seqs, batch, t)];
     const int i = t - sq.y;
-    const size_t tile = (size_t)sq.z + (size_t)h * sq.w + i / kTile;
-    const int r = i % kTile;
-    const float *tb = acc + tile * K * (C4 * kTile * 4);
-    float4 v = *reinterpret_cast<const float4 *>(tb + ((size_t)c4 * kTile + r) * 4);
-    if constexpr (K == 2) {
-      if ((causal ? i / kTile + 1 : sq.w) > 1) {
-        const float4 w = *reinterpret_cast<const float4 *>(tb + ((size_t)(C4 + c4) * kTile + r) * 4);
-        v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
-      }
-    }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t *>(&lo);
-    packed.y = *reinterpret_cast<uint32_t *>(&hi);
-    *reinterpret_cast<uint2 *>(dq + row * D + 4 * c4) = packed;
+    const size_t r = ((size_t)sq.z + (size_t)h * sq.w) * kTile + i;
+    dvec[r] = acc;
+    lse2[r] = lse[(size_t)sq.y * H + (size_t)h * sq.x + i] * kLog2e;
+  });
+}
+
+// The same per tile of a packed batch: tile t of the group's per-tile arrays belongs to
+// the last sequence whose first tile is <= t.
+template <int D, int K>
+__global__ void __launch_bounds__(256) dq_convert_varlen_kernel(
+    const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, float scale,
+    const int4 *__restrict__ seqs, int batch, int T, int H, int causal) {
+  __shared__ __align__(16) uint8_t st[ConvTile<D>::kBytes];
+  (void)T;
+  const int t = blockIdx.x;
+  int lo = 0, hi = batch;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (seqs[mid].z <= t) lo = mid;
+    else hi = mid;
   }
+  const int4 sq = seqs[lo];  // {S_b, first token, first tile, N_b}
+  const int local = t - sq.z;
+  const int h = local / sq.w, i = local % sq.w;
+  conv_tile_load<D, K>(acc + (size_t)t * K * (kTile * D), (causal ? i + 1 : sq.w) > 1 ? K : 1,
+                       scale, st);
+  __syncthreads();
+  const int rows = sq.x - i * kTile < kTile ? sq.x - i * kTile : kTile;
+  conv_tile_store<D>(st, dq + (((size_t)sq.y + (size_t)i * kTile) * H + h) * D, (size_t)H * D,
+                     rows);
 }
 
 int grid_for(long long work, int per_block, int cap) {
@@ -195,7 +257,7 @@ cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
                               float *dvec, float *lse2, int B, int S, int H, int D,
                               cudaStream_t stream) {
   const long long rows = (long long)B * S * H;
-  const int grid = grid_for(rows, 8, 152 * 16);
+  const int grid = grid_for(rows, kPreRowsPerBlock / (D == 64 ? 1 : 2), 152 * 16);
   if (D == 64)
     preprocess_kernel<64><<<grid, 256, 0, stream>>>(o, dout, lse, dvec, lse2, B, S, H);
   else
@@ -205,19 +267,21 @@ cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
 
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B, int S,
                               int H, int D, int strands, int causal, cudaStream_t stream) {
-  const long long work = (long long)B * H * ((S + kTile - 1) / kTile) * kTile * (D / 4);
-  const int grid = grid_for(work, 256, 152 * 32);
-  if (D == 64) {
-    if (strands == 2)
-      dq_convert_kernel<64, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
+  const long long tiles = (long long)B * H * ((S + kTile - 1) / kTile);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (strands == 2) {
+    const int grid = grid_for(tiles * kTile * (D / 4), 256, 152 * 32);
+    if (D == 64)
+      dq_convert2_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
     else
-      dq_convert_kernel<64, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
-  } else {
-    if (strands == 2)
-      dq_convert_kernel<128, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
-    else
-      dq_convert_kernel<128, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
+      dq_convert2_kernel<128><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
+    return cudaGetLastError();
   }
+  const int grid = (int)tiles;
+  if (D == 64)
+    dq_convert_kernel<64, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
+  else
+    dq_convert_kernel<128, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
   return cudaGetLastError();
 }
 
@@ -231,7 +295,7 @@ cudaError_t launch_preprocess_varlen(const __nv_bfloat16 *o, const __nv_bfloat16
                                      const float *lse, float *dvec, float *lse2, const int4 *seqs,
                                      int batch, int T, int H, int D, cudaStream_t stream) {
   const long long rows = (long long)T * H;
-  const int grid = grid_for(rows, 8, 152 * 16);
+  const int grid = grid_for(rows, kPreRowsPerBlock / (D == 64 ? 1 : 2), 152 * 16);
   if (D == 64)
     preprocess_varlen_kernel<64><<<grid, 256, 0, stream>>>(o, dout, lse, dvec, lse2, seqs, batch,
                                                            T, H);
@@ -242,22 +306,23 @@ cudaError_t launch_preprocess_varlen(const __nv_bfloat16 *o, const __nv_bfloat16
 }
 
 cudaError_t launch_dq_convert_varlen(const float *dqacc, __nv_bfloat16 *dq, float scale,
-                                     const int4 *seqs, int batch, int T, int H, int D,
+                                     const int4 *seqs, int batch, int ntiles, int H, int D,
                                      int strands, int causal, cudaStream_t stream) {
-  const long long work = (long long)T * H * (D / 4);
-  const int grid = grid_for(work, 256, 152 * 32);
+  if (ntiles <= 0) return cudaSuccess;
   if (D == 64) {
     if (strands == 2)
-      dq_convert_varlen_kernel<64, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T, H, causal);
+      dq_convert_varlen_kernel<64, 2><<<ntiles, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch,
+                                                                  ntiles, H, causal);
     else
-      dq_convert_varlen_kernel<64, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T, H, causal);
+      dq_convert_varlen_kernel<64, 1><<<ntiles, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch,
+                                                                  ntiles, H, causal);
   } else {
     if (strands == 2)
-      dq_convert_varlen_kernel<128, 2><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T,
-                                                                 H, causal);
+      dq_convert_varlen_kernel<128, 2><<<ntiles, 256, 0, stream>>>(dqacc, dq, scale, seqs,
+                                                                   batch, ntiles, H, causal);
     else
-      dq_convert_varlen_kernel<128, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch, T,
-                                                                 H, causal);
+      dq_convert_varlen_kernel<128, 1><<<ntiles, 256, 0, stream>>>(dqacc, dq, scale, seqs,
+                                                                   batch, ntiles, H, causal);
   }
   return cudaGetLastError();
 }

@@ -123,7 +123,7 @@ cudaError_t launch_preprocess_varlen(const __nv_bfloat16 *o, const __nv_bfloat16
                                      const float *lse, float *dvec, float *lse2, const int4 *seqs,
                                      int batch, int T, int H, int D, cudaStream_t stream);
 cudaError_t launch_dq_convert_varlen(const float *dqacc, __nv_bfloat16 *dq, float scale,
-                                     const int4 *seqs, int batch, int T, int H, int D,
+                                     const int4 *seqs, int batch, int ntiles, int H, int D,
                                      int strands, int causal, cudaStream_t stream);
 // Strands a dQ tile's accumulation is split into (DASH_SCHED_SHIFT_DUAL: 2), at most:
 constexpr int kMaxStrands = 2;
