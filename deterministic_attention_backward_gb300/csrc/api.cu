@@ -304,7 +304,7 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
       return DASH_ERR_CUDA;
     if (dash::launch_preprocess(static_cast<const __nv_bfloat16 *>(o),
                                 static_cast<const __nv_bfloat16 *>(dout), lse, w.dvec, w.lse2, B,
-                                S, H, D, s) != cudaSuccess)
+                                S, H, D, w.status, g_wait_ns.load(), s) != cudaSuccess)
       return DASH_ERR_CUDA;
   }
   if (!(stages & (DASH_BWD_TILES | DASH_BWD_EPILOGUE))) return DASH_OK;
@@ -552,7 +552,8 @@ static dash_status_t bwd_varlen_group(const VarlenGroup &g, const int *cu, const
   if (dash::launch_varlen_setup(t, seqs, wprefix, s) != cudaSuccess ||
       dash::launch_preprocess_varlen(static_cast<const bf *>(o) + qo,
                                      static_cast<const bf *>(dout) + qo, lse + (size_t)g.tok0 * H,
-                                     w.dvec, w.lse2, seqs, n, T, H, D, s) != cudaSuccess)
+                                     w.dvec, w.lse2, seqs, n, T, H, D, w.status,
+                                     g_wait_ns.load(), s) != cudaSuccess)
     return DASH_ERR_CUDA;
   dash::BwdParams p{};
   p.lse2 = w.lse2;

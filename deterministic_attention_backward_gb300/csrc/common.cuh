@@ -100,7 +100,8 @@ cudaError_t launch_fwd(int D, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
                               const float *lse, float *dvec, float *lse2, int B, int S, int H,
-                              int D, cudaStream_t stream);
+                              int D, uint32_t *status, unsigned long long wait_ns,
+                              cudaStream_t stream);
 // dQ = bf16(scale * (strand 0 + ... + strand K-1)) for every row < S.  A strand s that
 // received no partial (a tile with s or fewer: query tile 0 of a causal mask, or N = 1) is
 // not read: the two-strand schedule stores each strand's first partial instead of clearing
@@ -121,7 +122,8 @@ cudaError_t launch_varlen_setup(const VarlenTable &t, int4 *seqs, int *wprefix,
 // preprocess and convert over a packed batch of T tokens (sequence table in device memory)
 cudaError_t launch_preprocess_varlen(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
                                      const float *lse, float *dvec, float *lse2, const int4 *seqs,
-                                     int batch, int T, int H, int D, cudaStream_t stream);
+                                     int batch, int T, int H, int D, uint32_t *status,
+                                     unsigned long long wait_ns, cudaStream_t stream);
 cudaError_t launch_dq_convert_varlen(const float *dqacc, __nv_bfloat16 *dq, float scale,
                                      const int4 *seqs, int batch, int ntiles, int H, int D,
                                      int strands, int causal, cudaStream_t stream);
