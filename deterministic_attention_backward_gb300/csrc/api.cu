@@ -347,7 +347,7 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
     return DASH_ERR_CUDA;
   if ((stages & DASH_BWD_EPILOGUE) &&
       dash::launch_dq_convert(w.dqacc, static_cast<__nv_bfloat16 *>(dq), sc, B, S, H, D, K, causal,
-                              s) != cudaSuccess)
+                              w.status, g_wait_ns.load(), s) != cudaSuccess)
     return DASH_ERR_CUDA;
   return DASH_OK;
 }
@@ -586,7 +586,8 @@ static dash_status_t bwd_varlen_group(const VarlenGroup &g, const int *cu, const
   if (dash::launch_bwd_varlen(D, ordered, causal, K > 1, tq, tk, tv, tdo, p, grid, s) !=
           cudaSuccess ||
       dash::launch_dq_convert_varlen(w.dqacc, static_cast<bf *>(dq) + qo, sc, seqs, n,
-                                     (int)g.ntiles, H, D, K, causal, s) != cudaSuccess)
+                                     (int)g.ntiles, H, D, K, causal, w.status, g_wait_ns.load(),
+                                     s) != cudaSuccess)
     return DASH_ERR_CUDA;
   return DASH_OK;
 }

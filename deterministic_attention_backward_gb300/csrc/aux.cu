@@ -142,29 +142,68 @@ struct ConvTile {
                                                // at most two rows per bank
   static constexpr int kBytes = kTile * kRowBytes;
 };
-// Sums `strands` strands of the tile at `tb` into shared memory `st` (bf16, scaled).
+// Sums `strands` strands of the tile at `tb` into shared memory `st` (bf16, scaled).  Each
+// strand is [D/4][128][4] fp32; it is brought in by bulk (TMA) copies of kConvCols
+// 4-column groups (16 KB) at a time, two passes in flight, and read back row-fastest
+// (conflict-free); `stage` holds 2 x K x 16 KB, `bar` two mbarriers.  A wait that runs out
+// records kErrMbarTimeout through `ab` and returns false.
+constexpr int kConvCols = 8;                              // 4-column groups per pass
+constexpr int kConvChunk = kConvCols * kTile * 16;         // bytes per strand per pass
 template <int D, int K>
-__device__ __forceinline__ void conv_tile_load(const float *__restrict__ tb, int strands,
-                                               float scale, uint8_t *st) {
+__device__ __forceinline__ bool conv_tile_load(const float *__restrict__ tb, int strands,
+                                               float scale, uint8_t *st, uint8_t *stage,
+                                               uint64_t *bar, const Abort &ab) {
   constexpr int C4 = D / 4;
-  constexpr int kStrand = C4 * kTile;  // float4 per strand
-  const float4 *src = reinterpret_cast<const float4 *>(tb);
-  for (int idx = threadIdx.x; idx < kStrand; idx += blockDim.x) {
-    float4 v = __ldcs(src + idx);
-    if constexpr (K == 2) {
-      if (strands > 1) {
-        const float4 w = __ldcs(src + kStrand + idx);
-        v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
-      }
-    }
-    const int c4 = idx / kTile, r = idx % kTile;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t *>(&lo);
-    packed.y = *reinterpret_cast<uint32_t *>(&hi);
-    *reinterpret_cast<uint2 *>(st + r * ConvTile<D>::kRowBytes + c4 * 8) = packed;
+  constexpr int kPasses = C4 / kConvCols;
+  constexpr size_t kStrandBytes = (size_t)C4 * kTile * 16;
+  auto issue = [&](int pass) {
+    uint8_t *dst = stage + (pass & 1) * (K * kConvChunk);
+    mbar_arrive_expect_tx(&bar[pass & 1], strands * kConvChunk);
+    for (int k = 0; k < strands; ++k)
+      bulk_load(dst + k * kConvChunk, reinterpret_cast<const uint8_t *>(tb) + k * kStrandBytes +
+                                          (size_t)pass * kConvChunk,
+                kConvChunk, &bar[pass & 1]);
+  };
+  if (threadIdx.x == 0) {
+    issue(0);
+    if (kPasses > 1) issue(1);
   }
+  for (int pass = 0; pass < kPasses; ++pass) {
+    const bool ok = mbar_wait(&bar[pass & 1], (pass >> 1) & 1, ab);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0)  // leave no copy in flight into shared memory
+        for (int q = pass; q < kPasses && q < pass + 2; ++q)
+          mbar_wait_drain(&bar[q & 1], (q >> 1) & 1, 100000000ull);
+      return false;
+    }
+    const float4 *s0 = reinterpret_cast<const float4 *>(stage + (pass & 1) * (K * kConvChunk));
+#pragma unroll
+    for (int j = 0; j < kConvCols * kTile / 256; ++j) {
+      const int idx = threadIdx.x + 256 * j;  // (4-column group within the pass, row)
+      float4 v = s0[idx];
+      if constexpr (K == 2) {
+        if (strands > 1) {
+          const float4 w = s0[kConvChunk / 16 + idx];
+          v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+        }
+      }
+      const int c4 = pass * kConvCols + idx / kTile, r = idx % kTile;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
+      uint2 packed;
+      packed.x = *reinterpret_cast<uint32_t *>(&lo);
+      packed.y = *reinterpret_cast<uint32_t *>(&hi);
+      *reinterpret_cast<uint2 *>(st + r * ConvTile<D>::kRowBytes + c4 * 8) = packed;
+    }
+    __syncthreads();  // every thread is done with this pass's stage
+    if (threadIdx.x == 0 && pass + 2 < kPasses) issue(pass + 2);
+  }
+  return true;
+}
+// Dynamic shared memory of a convert CTA: two passes of K strands, the bf16 tile, barriers.
+template <int D, int K>
+constexpr int conv_smem_bytes() {
+  return 2 * K * kConvChunk + ConvTile<D>::kBytes + 32;
 }
 // Writes rows [0, rows) of the shared tile; row r goes to dst + r * row_stride (elements).
 template <int D>
@@ -178,49 +217,24 @@ __device__ __forceinline__ void conv_tile_store(const uint8_t *st, __nv_bfloat16
   }
 }
 
-// Two strands: one thread per 4 output elements, the 4-column chunk fastest so a warp
-// writes contiguous bf16 rows (measured faster than the per-tile form when both strands are
-// read: 77 vs 81 us for 16k tokens x 16 heads at D = 128).
-template <int D>
-__global__ void __launch_bounds__(256) dq_convert2_kernel(const float *__restrict__ acc,
-                                                          __nv_bfloat16 *__restrict__ dq,
-                                                          float scale, int B, int S, int H,
-                                                          int causal) {
-  constexpr int C4 = D / 4;
-  const int N = (S + kTile - 1) / kTile;
-  const long long total = (long long)B * H * N * kTile * C4;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int c4 = (int)(idx % C4);
-    const int r = (int)((idx / C4) % kTile);
-    const long long t = idx / ((long long)C4 * kTile);  // (b*H + h)*N + i
-    const int i = (int)(t % N);
-    const long long bh = t / N;
-    const int h = (int)(bh % H);
-    const int b = (int)(bh / H);
-    if (i * kTile + r >= S) continue;  // padding rows of a partial last tile
-    const float *tb = acc + t * 2 * (C4 * kTile * 4);
-    float4 v = *reinterpret_cast<const float4 *>(tb + ((size_t)c4 * kTile + r) * 4);
-    if ((causal ? i + 1 : N) > 1) {  // strand 1, when the tile has a second partial
-      const float4 w = *reinterpret_cast<const float4 *>(tb + ((size_t)(C4 + c4) * kTile + r) * 4);
-      v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
-    }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t *>(&lo);
-    packed.y = *reinterpret_cast<uint32_t *>(&hi);
-    *reinterpret_cast<uint2 *>(dq + (((size_t)b * S + (size_t)i * kTile + r) * H + h) * D +
-                               4 * c4) = packed;
-  }
-}
-
 template <int D, int K>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
                                                          __nv_bfloat16 *__restrict__ dq,
                                                          float scale, int B, int S, int H,
-                                                         int causal) {
-  __shared__ __align__(16) uint8_t st[ConvTile<D>::kBytes];
+                                                         int causal, uint32_t *status,
+                                                         unsigned long long wait_ns) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint8_t *st = sm + 2 * K * kConvChunk;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(st + ConvTile<D>::kBytes);
+  int *s_abort = reinterpret_cast<int *>(bar + 2);
+  const Abort ab{s_abort, status, wait_ns};
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
   const int N = (S + kTile - 1) / kTile;
   const long long t = blockIdx.x;  // (b*H + h)*N + i
   const int i = (int)(t % N);
@@ -228,9 +242,9 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
   const int h = (int)(bh % H);
   const int b = (int)(bh / H);
   // a strand that received no partial is not read (tile with a single partial)
-  conv_tile_load<D, K>(acc + t * K * (size_t)(kTile * D), (causal ? i + 1 : N) > 1 ? K : 1,
-                       scale, st);
-  __syncthreads();
+  if (!conv_tile_load<D, K>(acc + t * K * (size_t)(kTile * D), (causal ? i + 1 : N) > 1 ? K : 1,
+                            scale, st, sm, bar, ab))
+    return;
   const int rows = S - i * kTile < kTile ? S - i * kTile : kTile;
   conv_tile_store<D>(st, dq + (((size_t)b * S + (size_t)i * kTile) * H + h) * D,
                      (size_t)H * D, rows);
@@ -278,9 +292,20 @@ __global__ void __launch_bounds__(256) preprocess_varlen_kernel(
 template <int D, int K>
 __global__ void __launch_bounds__(256) dq_convert_varlen_kernel(
     const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq, float scale,
-    const int4 *__restrict__ seqs, int batch, int T, int H, int causal) {
-  __shared__ __align__(16) uint8_t st[ConvTile<D>::kBytes];
-  (void)T;
+    const int4 *__restrict__ seqs, int batch, int H, int causal, uint32_t *status,
+    unsigned long long wait_ns) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint8_t *st = sm + 2 * K * kConvChunk;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(st + ConvTile<D>::kBytes);
+  int *s_abort = reinterpret_cast<int *>(bar + 2);
+  const Abort ab{s_abort, status, wait_ns};
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
   const int t = blockIdx.x;
   int lo = 0, hi = batch;
   while (hi - lo > 1) {
@@ -291,9 +316,9 @@ __global__ void __launch_bounds__(256) dq_convert_varlen_kernel(
   const int4 sq = seqs[lo];  // {S_b, first token, first tile, N_b}
   const int local = t - sq.z;
   const int h = local / sq.w, i = local % sq.w;
-  conv_tile_load<D, K>(acc + (size_t)t * K * (kTile * D), (causal ? i + 1 : sq.w) > 1 ? K : 1,
-                       scale, st);
-  __syncthreads();
+  if (!conv_tile_load<D, K>(acc + (size_t)t * K * (kTile * D),
+                            (causal ? i + 1 : sq.w) > 1 ? K : 1, scale, st, sm, bar, ab))
+    return;
   const int rows = sq.x - i * kTile < kTile ? sq.x - i * kTile : kTile;
   conv_tile_store<D>(st, dq + (((size_t)sq.y + (size_t)i * kTile) * H + h) * D, (size_t)H * D,
                      rows);
@@ -327,24 +352,30 @@ cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
   return cudaGetLastError();
 }
 
+template <int D, int K>
+cudaError_t conv_launch(int grid, cudaStream_t stream, const float *dqacc, __nv_bfloat16 *dq,
+                        float scale, int B, int S, int H, int causal, uint32_t *status,
+                        unsigned long long wait_ns) {
+  constexpr int kSmem = conv_smem_bytes<D, K>();
+  cudaError_t e = cudaFuncSetAttribute(dq_convert_kernel<D, K>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  dq_convert_kernel<D, K><<<grid, 256, kSmem, stream>>>(dqacc, dq, scale, B, S, H, causal, status,
+                                                        wait_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B, int S,
-                              int H, int D, int strands, int causal, cudaStream_t stream) {
+                              int H, int D, int strands, int causal, uint32_t *status,
+                              unsigned long long wait_ns, cudaStream_t stream) {
   const long long tiles = (long long)B * H * ((S + kTile - 1) / kTile);
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (strands == 2) {
-    const int grid = grid_for(tiles * kTile * (D / 4), 256, 152 * 32);
-    if (D == 64)
-      dq_convert2_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
-    else
-      dq_convert2_kernel<128><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
-    return cudaGetLastError();
-  }
   const int grid = (int)tiles;
   if (D == 64)
-    dq_convert_kernel<64, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
-  else
-    dq_convert_kernel<128, 1><<<grid, 256, 0, stream>>>(dqacc, dq, scale, B, S, H, causal);
-  return cudaGetLastError();
+    return strands == 2 ? conv_launch<64, 2>(grid, stream, dqacc, dq, scale, B, S, H, causal, status, wait_ns)
+                        : conv_launch<64, 1>(grid, stream, dqacc, dq, scale, B, S, H, causal, status, wait_ns);
+  return strands == 2 ? conv_launch<128, 2>(grid, stream, dqacc, dq, scale, B, S, H, causal, status, wait_ns)
+                      : conv_launch<128, 1>(grid, stream, dqacc, dq, scale, B, S, H, causal, status, wait_ns);
 }
 
 cudaError_t launch_varlen_setup(const VarlenTable &t, int4 *seqs, int *wprefix,
@@ -367,26 +398,29 @@ cudaError_t launch_preprocess_varlen(const __nv_bfloat16 *o, const __nv_bfloat16
   return cudaGetLastError();
 }
 
+template <int D, int K>
+cudaError_t conv_varlen_launch(int ntiles, cudaStream_t stream, const float *dqacc,
+                               __nv_bfloat16 *dq, float scale, const int4 *seqs, int batch, int H,
+                               int causal, uint32_t *status, unsigned long long wait_ns) {
+  constexpr int kSmem = conv_smem_bytes<D, K>();
+  cudaError_t e = cudaFuncSetAttribute(dq_convert_varlen_kernel<D, K>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  dq_convert_varlen_kernel<D, K><<<ntiles, 256, kSmem, stream>>>(dqacc, dq, scale, seqs, batch, H,
+                                                                 causal, status, wait_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dq_convert_varlen(const float *dqacc, __nv_bfloat16 *dq, float scale,
                                      const int4 *seqs, int batch, int ntiles, int H, int D,
-                                     int strands, int causal, cudaStream_t stream) {
+                                     int strands, int causal, uint32_t *status,
+                                     unsigned long long wait_ns, cudaStream_t stream) {
   if (ntiles <= 0) return cudaSuccess;
-  if (D == 64) {
-    if (strands == 2)
-      dq_convert_varlen_kernel<64, 2><<<ntiles, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch,
-                                                                  ntiles, H, causal);
-    else
-      dq_convert_varlen_kernel<64, 1><<<ntiles, 256, 0, stream>>>(dqacc, dq, scale, seqs, batch,
-                                                                  ntiles, H, causal);
-  } else {
-    if (strands == 2)
-      dq_convert_varlen_kernel<128, 2><<<ntiles, 256, 0, stream>>>(dqacc, dq, scale, seqs,
-                                                                   batch, ntiles, H, causal);
-    else
-      dq_convert_varlen_kernel<128, 1><<<ntiles, 256, 0, stream>>>(dqacc, dq, scale, seqs,
-                                                                   batch, ntiles, H, causal);
-  }
-  return cudaGetLastError();
+  if (D == 64)
+    return strands == 2 ? conv_varlen_launch<64, 2>(ntiles, stream, dqacc, dq, scale, seqs, batch, H, causal, status, wait_ns)
+                        : conv_varlen_launch<64, 1>(ntiles, stream, dqacc, dq, scale, seqs, batch, H, causal, status, wait_ns);
+  return strands == 2 ? conv_varlen_launch<128, 2>(ntiles, stream, dqacc, dq, scale, seqs, batch, H, causal, status, wait_ns)
+                      : conv_varlen_launch<128, 1>(ntiles, stream, dqacc, dq, scale, seqs, batch, H, causal, status, wait_ns);
 }
 
 }  // namespace dash

@@ -107,7 +107,8 @@ cudaError_t launch_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
 // not read: the two-strand schedule stores each strand's first partial instead of clearing
 // the accumulator.
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, float scale, int B,
-                              int S, int H, int D, int strands, int causal, cudaStream_t stream);
+                              int S, int H, int D, int strands, int causal, uint32_t *status,
+                              unsigned long long wait_ns, cudaStream_t stream);
 
 // Packed variable-length batches: the sequence table (at most kMaxVarlenSeqs sequences) is
 // written into the workspace by a one-block kernel that receives it as its parameter.
@@ -126,7 +127,8 @@ cudaError_t launch_preprocess_varlen(const __nv_bfloat16 *o, const __nv_bfloat16
                                      unsigned long long wait_ns, cudaStream_t stream);
 cudaError_t launch_dq_convert_varlen(const float *dqacc, __nv_bfloat16 *dq, float scale,
                                      const int4 *seqs, int batch, int ntiles, int H, int D,
-                                     int strands, int causal, cudaStream_t stream);
+                                     int strands, int causal, uint32_t *status,
+                                     unsigned long long wait_ns, cudaStream_t stream);
 // Strands a dQ tile's accumulation is split into (DASH_SCHED_SHIFT_DUAL: 2), at most:
 constexpr int kMaxStrands = 2;
 
