@@ -166,10 +166,11 @@ bool sched_known(int sched) {
 // DASH_SCHED_SHIFT_DUAL shares.
 int resolve_sched(int sched, int mask, int D, int N, int G) {
   if (sched != DASH_SCHED_AUTO) return sched;
+  (void)mask;
+  (void)D;
   (void)N;
   (void)G;
-  if (mask == DASH_MASK_FULL || D == 128) return DASH_SCHED_SHIFT_DUAL;
-  return DASH_SCHED_SHIFT_FILL;
+  return DASH_SCHED_SHIFT_DUAL;
 }
 
 // False when plain SHIFT cannot have every worker of a head resident at once.  The packed

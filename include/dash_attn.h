@@ -91,16 +91,12 @@ typedef enum { DASH_MASK_FULL = 0, DASH_MASK_CAUSAL = 1 } dash_mask_t;
  *  DASH_SCHED_AUTO       -- the deterministic schedule that measured fastest on GB300 for
  *                           the mask, head dim, tile count N and group size G
  *                           (dash_sched_resolve names it): the pages leave the choice to the
- *                           user.  Table, from whole-call timings (full mask H16 and causal
- *                           H32 at D = 128 and 64, S = 512 .. 16384, GQA 4:1; N and G did not
- *                           change the winner):
- *                             full mask                           -> SHIFT_DUAL (D = 128: +12 %
- *                                                                    at N = 4, +16 % at N = 128;
- *                                                                    D = 64: +11 % at N = 4)
- *                             causal, D = 128                     -> SHIFT_DUAL (+1-3 % at
- *                                                                    N = 4..16, +8 % GQA N = 64)
- *                             causal, D = 64                      -> SHIFT_FILL (+1-12 %; equal
- *                                                                    at N = 4)
+ *                           user.  From whole-call timings (full mask H16 and causal H32 at
+ *                           D = 128 and 64, S = 512 .. 16384, GQA 4:1) one schedule wins every
+ *                           measured point: SHIFT_DUAL (against SHIFT_FILL: full mask +12 % at
+ *                           N = 4, +19 % at N = 128; causal D = 128 +1-3 %, GQA +10 %; causal
+ *                           D = 64 +2.5-4 %).  The mask, D, N and G remain arguments of
+ *                           dash_sched_resolve for future entries.
  *  DASH_SCHED_SHIFT_DUAL -- packed Shift Scheduling (the SHIFT_FILL traversal, grid and ranks)
  *                           with each dQ tile accumulated in two strands: the partial of rank
  *                           r is added into strand r mod 2 as that strand's (r div 2)-th

@@ -3,7 +3,8 @@ runs of every deterministic schedule give bit-identical dQ, dK, dV, idle and whi
 kernels load the GPU from a second stream, at both head dims and at 128 tiles per head;
 after a run every dQ tile's ordering semaphore (each strand's, for the two-strand schedule)
 holds exactly the number of partials it received (every partial went through its turn, none
-was skipped or added twice); and the
+was skipped or added twice; four releases per partial where each epilogue warp releases its
+own reductions); and the
 ordered tile kernel starts only once all of its CTAs can be resident,
 so SMs held by another kernel delay it instead of leaving its workers waiting on CTAs that
 cannot start."""
@@ -122,6 +123,9 @@ def test_every_partial_takes_its_turn(dash, shape, causal):
     for sched in scheds_for(shape[4]):
         K = dash.STRANDS[sched]
         want = np.stack([np.where(n > s, (n - s + K - 1) // K, 0) for s in range(K)], axis=-1)
+        # the causal two-strand kernel at D = 64 counts one release per epilogue warp (4)
+        if sched == "shift_dual" and causal and shape[4] == 64:
+            want = want * 4
         p.run(sched)
         p.dash.status(p.ws)
         sem = p.semaphores(K).cpu().numpy()
