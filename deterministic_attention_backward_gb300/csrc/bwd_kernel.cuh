@@ -49,7 +49,8 @@
 //   warps 4-11  two softmax-gradient warpgroups; warpgroup w handles query columns
 //               [64w, 64w+64) of the tile, thread = KV row (TMEM lane)
 //   warps 12-15 epilogue warpgroup: dQ partial TMEM -> ordered/atomic fp32 reduction in
-//               global memory; dK/dV TMEM -> bf16 at the end of each segment
+//               global memory; at D = 64 also dK/dV TMEM -> bf16 at the end of each
+//               segment (at D = 128 the softmax-gradient warpgroups drain dK and dV)
 // TMEM columns: S^T then P^T [0,128), dP^T then dS^T [128,256), dK [256,256+D), dV [256+D,256+2D);
 // the dQ partial reuses [128,256) at D=128 and has its own columns [384,448) at D=64.
 #pragma once
@@ -458,6 +459,9 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
         }
         if (!ok) break;
         mma_commit_e(&bar.empty[it % L::kStages]);
+        // D = 128: the segment's dK_j, dV_j are complete once its last G3 and G4 are, and
+        // the softmax-gradient warps drain them while G5 runs
+        if (D == 128 && st == nsteps - 1) mma_commit_e(bar.dkv_full);
         if (L::kDQOwnCols && it > 0) {
           if (!mbar_wait_warp(bar.dq_empty, (it - 1) & 1, ab)) {
             ok = false;
@@ -474,7 +478,7 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
         DASH_TRACE(p, 5);
         if (st == nsteps - 1) {
           mma_commit_e(bar.kv_empty);
-          mma_commit_e(bar.dkv_full);
+          if (D == 64) mma_commit_e(bar.dkv_full);
         }
       }
       ++seg_it;
@@ -502,7 +506,7 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const int c0 = x * 64;
   uint8_t *ds_row = smem + L::offDS + x * kBoxBytes + r * 128;
-  uint32_t it = 0;
+  uint32_t it = 0, seg_it = 0;
   bool ok = true;
   const Plan pl = cta_plan<MODE>(p);
   for (int u = pl.first; ok && u < pl.nunits; u += pl.stride) {
@@ -643,6 +647,49 @@ __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tme
             if (warp == 4 + 4 * x) DASH_TRACE(p, 9 + 4 * x);
           }
         }
+      }
+      if (!ok) break;
+      // segment end, D = 128: warpgroup 0 takes dK_j (scaled), warpgroup 1 dV_j, to bf16.
+      // The two warpgroups are otherwise idle here (the next segment's S^T needs its K_j),
+      // while the epilogue warpgroup still adds the segment's last dQ partial; drained by the
+      // epilogue, dK/dV would wait behind those reductions and hold the next segment's G3
+      // (measured: +4.5 % at S = 512, +1.5 % at 4k, full mask).  At D = 64, where these
+      // warps bound the step, the epilogue keeps the drain (-1.3 % there otherwise).
+      if constexpr (D == 128) {
+        if (!mbar_wait_warp(bar.dkv_full, seg_it & 1, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tcol = x == 0 ? L::tDK : L::tDV;
+        const float mul = x == 0 ? p.scale : 1.f;
+        __nv_bfloat16 *dst = (x == 0 ? p.dk : p.dv) +
+                             ((un.tok0 + (size_t)kv * kTile + r) * p.Hkv + un.hkv) * D;
+        const bool keep = kv * kTile + r < un.S;  // rows past S belong to no key
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t vv[32], pk2[16];
+          tmem_ld32(tmem + lane_off + tcol + ch * 32, vv);
+          tmem_ld_wait();
+          if (ch == D / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar.dkv_empty);
+          }
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            pk2[m] = pack_bf16(__uint_as_float(vv[2 * m]) * mul,
+                               __uint_as_float(vv[2 * m + 1]) * mul);
+          if (keep) {
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              d4[j] = make_uint4(pk2[4 * j], pk2[4 * j + 1], pk2[4 * j + 2], pk2[4 * j + 3]);
+          }
+        }
+        ++seg_it;
+      } else {
+        (void)seg_it;
       }
     }
   }
@@ -802,7 +849,6 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
     named_bar_sync(1, 128);
     return decision[dec++ & 1];
   };
-  auto agree = [&](bool mine) -> bool { return agree_int(mine ? 1 : 0) != 0; };
   const volatile int *ranks = reinterpret_cast<const volatile int *>(smem + L::offRanks);
   constexpr bool kBulk = L::kBulkDQ && !DET;
   const Plan pl = cta_plan<MODE>(p);
@@ -935,42 +981,48 @@ __device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, c
         }
       }
       if (!ok) break;
-      // segment end: dK_j (scaled) and dV_j to bf16
-      if (!agree(et == 0 ? mbar_wait(bar.dkv_full, seg_it & 1, ab) : true)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const size_t orow = ((un.tok0 + kv * kTile + r) * p.Hkv + un.hkv) * D;
+      if constexpr (D == 64) {  // segment end: dK_j (scaled) and dV_j to bf16
+        int got = 1;
+        if (et == 0) got = mbar_wait(bar.dkv_full, seg_it & 1, ab) ? 1 : 0;
+        if (!agree_int(got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const size_t orow = ((un.tok0 + (size_t)kv * kTile + r) * p.Hkv + un.hkv) * D;
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t kk[32], vv[32];
-        tmem_ld32(tmem + lane_off + L::tDK + ch * 32, kk);
-        tmem_ld32(tmem + lane_off + L::tDV + ch * 32, vv);
-        tmem_ld_wait();
-        if (ch == D / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar.dkv_empty);
-        }
-        uint32_t kp[16], vp[16];
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t kk[32], vv[32];
+          tmem_ld32(tmem + lane_off + L::tDK + ch * 32, kk);
+          tmem_ld32(tmem + lane_off + L::tDV + ch * 32, vv);
+          tmem_ld_wait();
+          if (ch == D / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar.dkv_empty);
+          }
+          uint32_t kp[16], vp[16];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          kp[m] = pack_bf16(__uint_as_float(kk[2 * m]) * p.scale,
-                            __uint_as_float(kk[2 * m + 1]) * p.scale);
-          vp[m] = pack_bf16(__uint_as_float(vv[2 * m]), __uint_as_float(vv[2 * m + 1]));
-        }
-        uint4 *dkp = reinterpret_cast<uint4 *>(p.dk + orow + ch * 32);
-        uint4 *dvp = reinterpret_cast<uint4 *>(p.dv + orow + ch * 32);
-        if (kv * kTile + r < un.S) {  // rows past S belong to no key
+          for (int m = 0; m < 16; ++m) {
+            kp[m] = pack_bf16(__uint_as_float(kk[2 * m]) * p.scale,
+                              __uint_as_float(kk[2 * m + 1]) * p.scale);
+            vp[m] = pack_bf16(__uint_as_float(vv[2 * m]), __uint_as_float(vv[2 * m + 1]));
+          }
+          uint4 *dkp = reinterpret_cast<uint4 *>(p.dk + orow + ch * 32);
+          uint4 *dvp = reinterpret_cast<uint4 *>(p.dv + orow + ch * 32);
+          if (kv * kTile + r < un.S) {  // rows past S belong to no key
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            dkp[j] = make_uint4(kp[4 * j], kp[4 * j + 1], kp[4 * j + 2], kp[4 * j + 3]);
-            dvp[j] = make_uint4(vp[4 * j], vp[4 * j + 1], vp[4 * j + 2], vp[4 * j + 3]);
+            for (int j = 0; j < 4; ++j) {
+              dkp[j] = make_uint4(kp[4 * j], kp[4 * j + 1], kp[4 * j + 2], kp[4 * j + 3]);
+              dvp[j] = make_uint4(vp[4 * j], vp[4 * j + 1], vp[4 * j + 2], vp[4 * j + 3]);
+            }
           }
         }
+        ++seg_it;
+      } else {
+        (void)kv;
+        (void)seg_it;
       }
-      ++seg_it;
     }
   }
   // leave no bulk reduction in flight
@@ -1010,7 +1062,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar.g5_done, 1);
     mbar_init(bar.dq_empty, 4);
     mbar_init(bar.dkv_full, 1);
-    mbar_init(bar.dkv_empty, 4);
+    mbar_init(bar.dkv_empty, D == 128 ? 8 : 4);  // the warps that drain dK/dV
     mbar_init(bar.drain, 1);
     if constexpr (L::kTurnRing) {
       for (int i = 0; i < L::kTurns; ++i) {
