@@ -216,3 +216,26 @@ def test_wait_limit_setting(L):
         assert dash.wait_limit() == pytest.approx(0.25)
     finally:
         dash.set_wait_limit(2.0)
+
+
+def test_varlen_workspace_spans_the_largest_packed_launch(L):
+    """More than 1024 non-empty sequences run as several packed launches that share the
+    workspace: its size is the largest launch's need (its tiles' arrays plus the table),
+    empty sequences taking no place in a launch."""
+    import ctypes as ct
+    table = 16 * 1024 + (4 * 1025 + 255) // 256 * 256
+    H, D = 2, 64
+    lens = [300] * 1024 + [0] * 5 + [3000] * 3   # launch 1: 1024 x 3 tiles; launch 2: 3 x 24
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    arr = (ct.c_int * len(cu))(*cu)
+    first = dash.bwd_workspace_bytes(1, 1024 * 3 * 128, H, D) + table
+    assert L.dash_attn_bwd_varlen_workspace_bytes(arr, len(lens), H, D) == first
+    lens2 = [300] * 10 + [0] * 2000 + [16000] * 2   # one launch: 10 x 3 + 2 x 125 tiles
+    cu2 = [0]
+    for n in lens2:
+        cu2.append(cu2[-1] + n)
+    arr2 = (ct.c_int * len(cu2))(*cu2)
+    want = dash.bwd_workspace_bytes(1, (10 * 3 + 2 * 125) * 128, H, D) + table
+    assert L.dash_attn_bwd_varlen_workspace_bytes(arr2, len(lens2), H, D) == want
