@@ -26,3 +26,15 @@ def test_reference_arm_prints_the_contract_line():
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "full_h16_d128"
+
+
+def test_varlen_workload_recipe():
+    """The packed-batch timing draws its sequence lengths log-uniformly in [lo, hi] from a
+    seeded generator: the same 64 lengths on every run."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a, b = bench.varlen_lengths(), bench.varlen_lengths()
+    cfg = bench.VARLEN
+    assert a == b and len(a) == cfg["n"]
+    assert all(cfg["lo"] <= n <= cfg["hi"] for n in a)
+    assert len(set(a)) > cfg["n"] // 2  # a spread of lengths, not one repeated value
