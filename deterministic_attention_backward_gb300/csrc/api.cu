@@ -190,6 +190,35 @@ float resolve_scale(float scale, int D) {
   return scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
 }
 
+// The tile kernel's parameters that uniform and packed batches fill alike: workspace
+// arrays, outputs, the order log, heads, mask, scale, wait limit (and the development
+// trace buffer).  The caller adds the batch geometry and the schedule.
+dash::BwdParams base_params(const BwdWorkspace &w, void *dk, void *dv, int *order_log,
+                            int log_stride, int H, int group, int causal, float sc) {
+  dash::BwdParams p{};
+  p.lse2 = w.lse2;
+  p.dvec = w.dvec;
+  p.dqacc = w.dqacc;
+  p.sem = w.sem;
+  p.status = w.status;
+  p.dk = static_cast<__nv_bfloat16 *>(dk);
+  p.dv = static_cast<__nv_bfloat16 *>(dv);
+  p.order_log = order_log;
+  p.log_stride = log_stride;
+  p.H = H;
+  p.Hkv = H / group;
+  p.G = group;
+  p.causal = causal;
+  p.wait_ns = g_wait_ns.load();
+  p.scale_log2 = sc * dash::kLog2e;
+  p.scale = sc;
+#ifdef DASH_TRACE_BUILD
+  p.trace = g_trace;
+  p.trace_cta = g_trace_cta;
+#endif
+  return p;
+}
+
 }  // namespace
 
 extern "C" {
@@ -309,37 +338,15 @@ static dash_status_t bwd_impl(const void *q, const void *k, const void *v, const
       return DASH_ERR_CUDA;
   }
   if (!(stages & (DASH_BWD_TILES | DASH_BWD_EPILOGUE))) return DASH_OK;
-  dash::BwdParams p{};
-  p.lse2 = w.lse2;
-  p.dvec = w.dvec;
-  p.dqacc = w.dqacc;
-  p.sem = w.sem;
-  p.status = w.status;
-  p.dk = static_cast<__nv_bfloat16 *>(dk);
-  p.dv = static_cast<__nv_bfloat16 *>(dv);
-  p.order_log = ordered ? order_log : nullptr;
-  p.log_stride = log_stride > 0 ? log_stride : N;
+  dash::BwdParams p = base_params(w, dk, dv, ordered ? order_log : nullptr,
+                                  log_stride > 0 ? log_stride : N, H, group, causal, sc);
   p.B = B;
   p.S = S;
-  p.H = H;
-  p.Hkv = Hkv;
-  p.G = group;
   p.N = N;
-  p.causal = causal;
   p.heads = B * Hkv;
   p.sched = plan.sched;
   p.workers = plan.workers;
   p.packed = plan.packed;
-  p.wait_ns = g_wait_ns.load();
-  p.scale_log2 = sc * dash::kLog2e;
-  p.scale = sc;
-#ifdef DASH_TRACE_BUILD
-  p.trace = g_trace;
-  p.trace_cta = g_trace_cta;
-#else
-  p.trace = nullptr;
-  p.trace_cta = 0;
-#endif
   if ((stages & DASH_BWD_TILES) &&
       dash::launch_bwd(D, ordered,
                        (causal ? (((N & 1) && plan.sched == dash::kShift) ? 2 : 1) : 0) |
@@ -556,33 +563,15 @@ static dash_status_t bwd_varlen_group(const VarlenGroup &g, const int *cu, const
                                      w.dvec, w.lse2, seqs, n, T, H, D, w.status,
                                      g_wait_ns.load(), s) != cudaSuccess)
     return DASH_ERR_CUDA;
-  dash::BwdParams p{};
-  p.lse2 = w.lse2;
-  p.dvec = w.dvec;
-  p.dqacc = w.dqacc;
-  p.sem = w.sem;
-  p.status = w.status;
-  p.dk = static_cast<bf *>(dk) + ko;
-  p.dv = static_cast<bf *>(dv) + ko;
-  p.order_log = ordered ? order_log : nullptr;
-  p.log_stride = log_stride;
+  dash::BwdParams p = base_params(w, static_cast<bf *>(dk) + ko, static_cast<bf *>(dv) + ko,
+                                  ordered ? order_log : nullptr, log_stride, H, group, causal,
+                                  sc);
   p.seqs = seqs;
   p.seq_wprefix = wprefix;
   p.batch = n;
   p.units = unit;
-  p.H = H;
-  p.Hkv = Hkv;
-  p.G = group;
-  p.causal = causal;
   p.sched = dash::kShift;
   p.packed = sched == DASH_SCHED_SHIFT_FILL || sched == DASH_SCHED_SHIFT_DUAL;
-  p.wait_ns = g_wait_ns.load();
-  p.scale_log2 = sc * dash::kLog2e;
-  p.scale = sc;
-#ifdef DASH_TRACE_BUILD
-  p.trace = g_trace;
-  p.trace_cta = g_trace_cta;
-#endif
   const int grid = unit < sms ? unit : sms;
   if (dash::launch_bwd_varlen(D, ordered, causal, K > 1, tq, tk, tv, tdo, p, grid, s) !=
           cudaSuccess ||
