@@ -81,13 +81,14 @@ __host__ __device__ constexpr bool varlen_of(int mode) { return (mode & 8) != 0;
 
 // Depth of the ring of mbarriers through which the semaphore poller hands a dQ tile's turn
 // to the epilogue (ordered variant): the poller runs at most this many steps ahead
-// (measured: 8 at D = 64, where steps are half as long; 4 at D = 128, 3 % ahead of 8).
-template <int D>
+// (measured: 8 at D = 64, where steps are half as long; at D = 128, 4 for the full mask
+// (1.5 % ahead of 8) and 8 for the causal mask (2 % ahead of 4)).
+template <int D, int MODE>
 struct Turns {
-  static constexpr int kN = (D == 64) ? 8 : 4;
+  static constexpr int kN = (D == 64 || (MODE & 3) != 0) ? 8 : 4;
 };
 
-template <int D, bool DET>
+template <int D, bool DET, int MODE>
 struct BwdLayout {
   static constexpr int kStages = (D == 64) ? (DET ? 4 : 3) : 2;
   // D = 64, atomic variant: the dQ partial goes out by one bulk (TMA) reduction from a
@@ -115,7 +116,7 @@ struct BwdLayout {
   // epilogue's reductions issued, for the releaser warp) and the ranks of the ring's steps
   // (misc words from offRanks).
   static constexpr bool kTurnRing = DET;
-  static constexpr int kTurns = Turns<D>::kN;
+  static constexpr int kTurns = Turns<D, MODE>::kN;
   static constexpr int kNumBars = 2 * kStages + 15 + (kTurnRing ? 3 * kTurns : 0);
   static constexpr int offMisc = offBar + kNumBars * 8;
   static constexpr int offRanks = offMisc + 32;
@@ -226,12 +227,12 @@ __device__ __forceinline__ size_t tile_of(const Unit &un, int h, int q) {
   return un.tiles0 + (size_t)h * un.N + q;
 }
 
-template <int D, bool DET>
+template <int D, bool DET, int MODE>
 struct Bars {
   uint64_t *full, *empty, *kv_full, *kv_empty, *s_full, *p_ready, *dp_full, *pds, *g5_done,
       *dq_empty, *dkv_full, *dkv_empty, *drain, *turn_full, *turn_empty, *added;
   __device__ explicit Bars(uint8_t *smem) {
-    using L = BwdLayout<D, DET>;
+    using L = BwdLayout<D, DET, MODE>;
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + L::offBar);
     full = b;
     empty = b + L::kStages;
@@ -271,8 +272,8 @@ __device__ __forceinline__ void load_rows(void *dst, const CUtensorMap *map, uin
 template <int D, bool DET, int MODE>
 __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                              const CUtensorMap *tdo, const BwdParams &p, uint8_t *smem,
-                             const Bars<D, DET> &bar, const Abort &ab) {
-  using L = BwdLayout<D, DET>;
+                             const Bars<D, DET, MODE> &bar, const Abort &ab) {
+  using L = BwdLayout<D, DET, MODE>;
   uint32_t it = 0, seg_it = 0;
   int last_full[L::kStages];
 #pragma unroll
@@ -352,9 +353,9 @@ __device__ void bwd_producer(const CUtensorMap *tq, const CUtensorMap *tk, const
 // softmax-gradient warps have written P^T over the current S^T columns, G3 and then the
 // next step's S^T product are issued, so both run while those warps compute dS.
 template <int D, bool DET, int MODE>
-__device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
+__device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET, MODE> &bar,
                         const Abort &ab) {
-  using L = BwdLayout<D, DET>;
+  using L = BwdLayout<D, DET, MODE>;
   constexpr uint32_t kIdescSS = make_idesc_bf16(128, 128, false, false);  // G1, G2
   constexpr uint32_t kIdescTS = make_idesc_bf16(128, D, false, true);     // G3, G4x
   constexpr uint32_t kIdescG5 = make_idesc_bf16(128, D, true, true);      // G5
@@ -497,8 +498,8 @@ __device__ void bwd_mma(const BwdParams &p, uint8_t *smem, uint32_t tmem, const 
 // just read; dS also goes to shared memory for G5.
 template <int D, bool DET, int MODE>
 __device__ void bwd_softmax_grad(const BwdParams &p, uint8_t *smem, uint32_t tmem,
-                                 const Bars<D, DET> &bar, const Abort &ab) {
-  using L = BwdLayout<D, DET>;
+                                 const Bars<D, DET, MODE> &bar, const Abort &ab) {
+  using L = BwdLayout<D, DET, MODE>;
   const int warp = warp_id(), lane = lane_id();
   const int x = (warp - 4) >> 2;  // query half: columns [64x, 64x + 64)
   const int quad = warp & 3;
@@ -727,11 +728,11 @@ __device__ __forceinline__ int step_rank(const BwdParams &p, const Plan &pl, con
 // thus overlap the computation of the dQ partial instead of following its drain.
 template <int D, bool DET, int MODE>
 __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &ab) {
-  using L = BwdLayout<D, DET>;
+  using L = BwdLayout<D, DET, MODE>;
   constexpr bool kDual = dual_of(MODE);
   volatile int *ranks = reinterpret_cast<volatile int *>(smem + L::offRanks);
   const int lane = lane_id();
-  const Bars<D, DET> bar(smem);
+  const Bars<D, DET, MODE> bar(smem);
   uint32_t it = 0;
   const Plan pl = cta_plan<MODE>(p);
   for (int u = pl.first; u < pl.nunits; u += pl.stride) {
@@ -786,9 +787,9 @@ __device__ void bwd_sem_poller(const BwdParams &p, uint8_t *smem, const Abort &a
 // epilogue, which goes on to drain the next dQ partial (measured: +16 % together with the
 // paced reductions at S = 16k, full mask; neither helps alone).
 template <int D, bool DET, int MODE>
-__device__ void bwd_releaser(const BwdParams &p, uint8_t *smem, const Bars<D, DET> &bar,
+__device__ void bwd_releaser(const BwdParams &p, uint8_t *smem, const Bars<D, DET, MODE> &bar,
                              const Abort &ab) {
-  using L = BwdLayout<D, DET>;
+  using L = BwdLayout<D, DET, MODE>;
   const int lane = lane_id();
   const volatile int *ranks = reinterpret_cast<const volatile int *>(smem + L::offRanks);
   uint32_t it = 0;
@@ -830,9 +831,9 @@ __device__ __forceinline__ int turn_code(int rank) {
 }
 
 template <int D, bool DET, int MODE>
-__device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET> &bar,
+__device__ void bwd_epilogue(const BwdParams &p, uint8_t *smem, uint32_t tmem, const Bars<D, DET, MODE> &bar,
                              const Abort &ab) {
-  using L = BwdLayout<D, DET>;
+  using L = BwdLayout<D, DET, MODE>;
   constexpr bool kDual = dual_of(MODE);
   const int warp = warp_id(), lane = lane_id();
   const int et = threadIdx.x - 12 * 32;  // 0..127
@@ -1035,13 +1036,13 @@ __global__ void __launch_bounds__(512, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const BwdParams p) {
-  using L = BwdLayout<D, DET>;
+  using L = BwdLayout<D, DET, MODE>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(p.status, kErrSmemAlign);
     return;
   }
-  const Bars<D, DET> bar(smem);
+  const Bars<D, DET, MODE> bar(smem);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L::offMisc);
   int *s_abort = reinterpret_cast<int *>(smem + L::offMisc + 4);
   const Abort ab{s_abort, p.status, p.wait_ns};
@@ -1118,7 +1119,7 @@ __global__ void __launch_bounds__(512, 1)
 template <int D, bool DET, int MODE>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &tdo, const BwdParams &p, int grid, cudaStream_t stream) {
-  using L = BwdLayout<D, DET>;
+  using L = BwdLayout<D, DET, MODE>;
   auto kern = bwd_kernel<D, DET, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
